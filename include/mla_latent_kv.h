@@ -1,0 +1,176 @@
+/*
+ * mla_latent_kv.h -- C ABI of the GB300 (sm_103a) MLA latent-KV decode library.
+ *
+ * The library runs the decode hot path of Multi-head Latent Attention after matrix absorption:
+ *
+ *   mla_absorb_q   q_nope [T,H,128] x W_UK_T [H,128,512] -> q [T,H,576] = [ql_nope || q_pe]
+ *   mla_decode     q [B,Sq,H,576] over a paged latent cache [num_blocks,64,576]
+ *                  -> o_latent [B,Sq,H,512], lse [B,Sq,H]   (MQA: all heads read one KV row)
+ *   mla_out_proj   o_latent [T,H,512] x W_UV [H,512,128] -> o [T,H,128]
+ *
+ * Sources, cited as [page, section]:
+ *   [vLLM-MLA]   "vLLM 源码完全拆解(三十七):MLA 注意力后端——矩阵吸收之后,576 维 latent KV
+ *                如何被四种内核读走" (vLLM source teardown 37: the MLA attention backend)
+ *   [TRT-TP]     "TensorRT-LLM 源码完全拆解(十二):注意力层的张量并行" (absorption section)
+ *   [Triton-MLA] "Triton und MLA: portable Attention und Latent-Space-Attention"
+ *
+ * Conventions shared by every call:
+ *   - All tensor arguments are DEVICE pointers owned by the caller, unless a parameter says
+ *     otherwise. The library never allocates, frees or synchronises inside these calls; every
+ *     launch is asynchronous on `stream` (NULL = the legacy default stream).
+ *   - Arguments are validated on the host before anything is launched. On any error the call
+ *     returns a non-zero mla_status, launches nothing, and mla_last_error_detail() (per host
+ *     thread) describes the failure. Unsupported shapes fail loudly; there is no fallback path
+ *     ([vLLM-MLA, multi-GPU section]: capability mismatches raise instead of degrading).
+ *   - Faults that only the device can see (a block-table entry outside [0, num_blocks), a
+ *     seq_len larger than max_blocks*64, a bounded wait that ran out) are OR-ed as MLA_DEV_*
+ *     bits into the optional int32 `dev_status` in device memory; the caller reads it after
+ *     synchronising. The kernels never trap.
+ *   - bf16 means IEEE bfloat16 bits; all layouts are row-major, last index fastest.
+ */
+#ifndef MLA_LATENT_KV_H
+#define MLA_LATENT_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* mla_stream_t;
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,         /* null pointer, negative size, inconsistent arguments */
+    MLA_ERR_UNSUPPORTED = 2,         /* valid but outside what the kernels implement */
+    MLA_ERR_WORKSPACE_TOO_SMALL = 3, /* split-KV workspace smaller than required */
+    MLA_ERR_CUDA = 4                 /* a CUDA runtime call failed (see detail string) */
+} mla_status;
+
+/* Cache row formats ([vLLM-MLA, cache shape section]):
+ *   MLA_KV_BF16            576 bf16 = 1152 bytes: [kv_c (512) || k_pe (64)]
+ *   MLA_KV_FP8_E4M3_SCALED 576 OCP-FP8-E4M3 bytes, then k_scale (fp32, byte 576) and v_scale
+ *                          (fp32, byte 580) = 584 bytes. K = e4m3 * k_scale over all 576 dims,
+ *                          V = e4m3 * v_scale over the first 512 dims. */
+typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3_SCALED = 1 } mla_kv_dtype;
+
+/* Element type of o_latent (decode output / out_proj input) and of o. */
+typedef enum { MLA_DT_F32 = 0, MLA_DT_BF16 = 1 } mla_dtype;
+
+/* DeepSeek-V3 MLA shape ([vLLM-MLA, model layer section]); the only shape implemented, as in
+ * the Cutlass and FlashMLA backends ([vLLM-MLA, Cutlass MLA and FlashMLA sections]). */
+#define MLA_KV_LORA_RANK 512
+#define MLA_ROPE_DIM 64
+#define MLA_HEAD_DIM 576 /* cached row / absorbed query width */
+#define MLA_NOPE_DIM 128
+#define MLA_V_DIM 128
+#define MLA_PAGE_SIZE 64
+#define MLA_MAX_HEADS 128
+
+/* Device status bits (OR-ed into *dev_status). */
+#define MLA_DEV_BAD_BLOCK_ID 0x1 /* a needed block_table entry was outside [0, num_blocks) */
+#define MLA_DEV_SEQ_TOO_LONG 0x2 /* seq_lens[b] > max_blocks * 64 or > max_seq_len */
+#define MLA_DEV_WAIT_TIMEOUT 0x4 /* a bounded pipeline wait expired; outputs are invalid */
+
+/* Human-readable name of a status. Never NULL. */
+const char* mla_status_string(mla_status s);
+
+/* Detail of the last failing call on this host thread ("" if none). Never NULL. */
+const char* mla_last_error_detail(void);
+
+/* Bytes of one cached token row: 1152 (bf16) or 584 (FP8), -1 for an unknown format
+ * ([vLLM-MLA, cache shape section]; [vLLM-MLA, numbers section]). Host only. */
+int64_t mla_kv_row_bytes(mla_kv_dtype kv_dtype);
+
+/* The Triton backend's split count ([vLLM-MLA, Triton MLA section], _compute_num_kv_splits):
+ * min(next_pow2(max(1, max_seq_len / 512)), 2 * sm_count). Host only; -1 if an argument is < 0
+ * or sm_count < 1. */
+int mla_default_num_splits(int max_seq_len, int sm_count);
+
+/* Effective split count mla_decode will use for a `num_splits` request on the current CUDA
+ * device:  > 0  that many splits (forced);
+ *            0  mla_default_num_splits(max_seq_len, SM count of the device);
+ *           -1  this library's own choice for GB300: the smallest count whose grid of
+ *               (B*Sq*splits) units fills whole waves of the device's SMs, capped by the
+ *               number of 64-token pages of the longest row.
+ * Returns -1 on invalid arguments or if the SM count cannot be queried. Host only, no sync. */
+int mla_resolve_num_splits(int num_splits, int B, int Sq, int H, int max_seq_len);
+
+/* Bytes of split-KV workspace mla_decode needs for `num_splits` resolved splits: 0 when
+ * num_splits == 1, else B*Sq*num_splits*H*(512 + 1)*4 rounded up to 256 (fp32 partial outputs
+ * and partial LSEs, [vLLM-MLA, Triton MLA section]: attn_logits (B, N, splits, 512 + 1), fp32
+ * because the LSE precision decides the merge). Host only. */
+size_t mla_decode_workspace_bytes(int B, int Sq, int H, int num_splits);
+
+/*
+ * Query absorption ([vLLM-MLA, two-algorithms section]: ql_nope = q_nope W_UK^T, concatenated
+ * with q_pe; [TRT-TP, absorption section]: fused_q = [q_nope W_kb^T || q_pe]):
+ *     q_out[t, h, l]       = sum_p q_nope[t, h, p] * W_UK_T[h, p, l]   (l < 512, fp32 accumulate,
+ *                                                                        rounded once to bf16)
+ *     q_out[t, h, 512 + r] = q_pe[t, h, r]                              (r < 64, copied)
+ *   q_nope  bf16, element (t, h, p) at q_nope[t*q_nope_stride_t + h*q_nope_stride_h + p]
+ *   q_pe    bf16, element (t, h, r) at q_pe[t*q_pe_stride_t + h*q_pe_stride_h + r]; may be NULL,
+ *           in which case q_out[..., 512:576] is left untouched
+ *   W_UK_T  bf16 [H, 128, 512] contiguous (vLLM's W_UK.permute(1, 2, 0))
+ *   q_out   bf16 [T, H, 576] contiguous; must not overlap the inputs
+ * Strides are in elements and must be multiples of 8 (16-byte rows for TMA); all pointers
+ * 16-byte aligned. 1 <= H <= 128, T >= 0 (T == 0 launches nothing).
+ */
+mla_status mla_absorb_q(const void* q_nope, int64_t q_nope_stride_t, int64_t q_nope_stride_h,
+                        const void* q_pe, int64_t q_pe_stride_t, int64_t q_pe_stride_h,
+                        const void* W_UK_T, void* q_out, int T, int H, mla_stream_t stream);
+
+/*
+ * Paged MQA decode over the latent cache ([vLLM-MLA, two-algorithms section]:
+ * o = SDPA([ql_nope, q_pe], [kv_c, k_pe], kv_c); [vLLM-MLA, FlashMLA section]: the cache is
+ * read as a single KV head; [Triton-MLA, Datenfluss]). For every request b, query row t < Sq and
+ * head h, with n = max(0, seq_lens[b] - (Sq - 1 - t)) visible tokens ([vLLM-MLA, Triton MLA
+ * section]: causal multi-token rows via per-row seq_len):
+ *     s_j          = scale * < q[b,t,h,0:576], K_j >                   j < n
+ *     lse[b,t,h]   = ln sum_j exp(s_j)                                 (natural log, scale inside)
+ *     o_latent[b,t,h,:] = sum_j exp(s_j - lse) * V_j                   (512 values)
+ * where row j of request b is cache[block_table[b, j / 64], j % 64, :], K_j is its 576 values
+ * and V_j its first 512 values (dequantised per row for the FP8 format). A row with n == 0
+ * gets o_latent = 0 and lse = -inf. `scale` is the caller's softmax scale; for DeepSeek-V3 it
+ * is 1/sqrt(192), not 1/sqrt(576) ([vLLM-MLA, two-algorithms section]).
+ *
+ *   q           bf16 [B, Sq, H, 576] contiguous (16-byte aligned)
+ *   kv_cache    [num_blocks, 64, row] bytes, row = mla_kv_row_bytes(kv_dtype) (16-byte aligned)
+ *   block_table int32 [B, max_blocks] contiguous; only entries j/64 for j < seq_lens[b] are read
+ *   seq_lens    int32 [B]: KV tokens of request b INCLUDING its Sq new ones (already written)
+ *   max_seq_len host upper bound of seq_lens (used for planning; exceeding it sets
+ *               MLA_DEV_SEQ_TOO_LONG and the row's output is undefined)
+ *   num_splits  split-KV request, see mla_resolve_num_splits (1 = no split, deterministic
+ *               per-row reduction order independent of the batch, [vLLM-MLA, FlashMLA section])
+ *   workspace   device scratch of >= mla_decode_workspace_bytes(B, Sq, H, resolved splits)
+ *               bytes (may be NULL when that is 0); contents on entry are ignored
+ *   o_latent    [B, Sq, H, 512] of o_dtype (fp32 recommended; bf16 rounds the result once)
+ *   lse         fp32 [B, Sq, H], may be NULL
+ *   dev_status  int32 device word or NULL; MLA_DEV_* bits are OR-ed into it, never cleared
+ * Limits: 1 <= H <= 128, Sq >= 1, B >= 0 (B == 0 launches nothing), page size 64.
+ */
+mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype, int64_t num_blocks,
+                      const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                      int max_seq_len, int B, int Sq, int H, float scale, int num_splits,
+                      void* workspace, size_t workspace_bytes, void* o_latent, mla_dtype o_dtype,
+                      float* lse, int32_t* dev_status, mla_stream_t stream);
+
+/*
+ * Output up-projection ([vLLM-MLA, two-algorithms section], _v_up_proj: per-head batched GEMM,
+ * written token-major):
+ *     o[t, h, v] = sum_l o_latent[t, h, l] * W_UV[h, l, v]      (512 -> 128, fp32 accumulate)
+ *   o_latent  [T, H, 512] contiguous, fp32 or bf16 (in_dtype)
+ *   W_UV      bf16 [H, 512, 128] contiguous (vLLM's W_UV.transpose(0, 1))
+ *   o         [T, H, 128] contiguous, fp32 or bf16 (out_dtype); must not overlap the inputs
+ * 1 <= H <= 128, T >= 0. Pointers 16-byte aligned.
+ */
+mla_status mla_out_proj(const void* o_latent, mla_dtype in_dtype, const void* W_UV, void* o,
+                        mla_dtype out_dtype, int T, int H, mla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_LATENT_KV_H */

@@ -1,0 +1,166 @@
+"""Python binding of the GB300 MLA latent-KV decode library (libmla_latent_kv.so).
+
+Argument marshalling only: every step of absorption, decode, split merge and output projection
+runs in the library's CUDA kernels. PyTorch supplies device memory and the current stream. If the
+native library has not been built, importing works but every call raises -- there is no
+fallback path. Build it with ``python -m mla_latent_kv_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libmla_latent_kv.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "mla_latent_kv.h")
+
+KV_BF16, KV_FP8 = 0, 1
+DT_F32, DT_BF16 = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA = range(5)
+DEV_BAD_BLOCK_ID, DEV_SEQ_TOO_LONG, DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
+L, R, D, P, V, PAGE, MAX_HEADS = 512, 64, 576, 128, 128, 64, 128
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"{status_string(status)}: {detail}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load the native library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"native library missing: {LIB_PATH} "
+                               "(build it with `python -m mla_latent_kv_gb300.build`)")
+        l = ctypes.CDLL(LIB_PATH)
+        i32, i64, vp, f32, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
+        l.mla_status_string.restype = ctypes.c_char_p
+        l.mla_status_string.argtypes = [i32]
+        l.mla_last_error_detail.restype = ctypes.c_char_p
+        l.mla_last_error_detail.argtypes = []
+        l.mla_kv_row_bytes.restype = i64
+        l.mla_kv_row_bytes.argtypes = [i32]
+        l.mla_default_num_splits.restype = i32
+        l.mla_default_num_splits.argtypes = [i32, i32]
+        l.mla_resolve_num_splits.restype = i32
+        l.mla_resolve_num_splits.argtypes = [i32, i32, i32, i32, i32]
+        l.mla_decode_workspace_bytes.restype = sz
+        l.mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        l.mla_absorb_q.restype = i32
+        l.mla_absorb_q.argtypes = [vp, i64, i64, vp, i64, i64, vp, vp, i32, i32, vp]
+        l.mla_decode.restype = i32
+        l.mla_decode.argtypes = [vp, vp, i32, i64, vp, i32, vp, i32, i32, i32, i32, f32, i32, vp, sz,
+                                 vp, i32, vp, vp, vp]
+        l.mla_out_proj.restype = i32
+        l.mla_out_proj.argtypes = [vp, i32, vp, vp, i32, i32, i32, vp]
+        _lib = l
+        return l
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/mla_latent_kv.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\*]+\s*\*?\s*(mla_\w+)\s*\(", text, re.M)))
+
+
+def status_string(status: int) -> str:
+    return lib().mla_status_string(int(status)).decode()
+
+
+def _check(status: int):
+    if status != OK:
+        raise MlaError(status, lib().mla_last_error_detail().decode())
+
+
+def row_bytes(kv_dtype: int) -> int:
+    return int(lib().mla_kv_row_bytes(kv_dtype))
+
+
+def default_num_splits(max_seq_len: int, sm_count: int) -> int:
+    return int(lib().mla_default_num_splits(max_seq_len, sm_count))
+
+
+def resolve_num_splits(num_splits: int, B: int, Sq: int, H: int, max_seq_len: int) -> int:
+    s = int(lib().mla_resolve_num_splits(num_splits, B, Sq, H, max_seq_len))
+    if s < 1:
+        raise MlaError(ERR_INVALID_ARG, "could not resolve num_splits")
+    return s
+
+
+def workspace_bytes(B: int, Sq: int, H: int, num_splits: int) -> int:
+    return int(lib().mla_decode_workspace_bytes(B, Sq, H, num_splits))
+
+
+# ----------------------------------------------------------------------------- torch front end
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def absorb_q(q_nope, q_pe, w_uk_t, out=None, stream=None):
+    """q_nope [T,H,128] bf16 (any token/head strides, unit stride inside a head), q_pe [T,H,64]
+    bf16 or None, W_UK_T [H,128,512] bf16 -> q [T,H,576] bf16."""
+    import torch
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    assert q_nope.stride(2) == 1 and w_uk_t.is_contiguous()
+    if out is None:
+        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q_nope.device)
+    spt, sph = (q_pe.stride(0), q_pe.stride(1)) if q_pe is not None else (0, 0)
+    _check(lib().mla_absorb_q(_p(q_nope), q_nope.stride(0), q_nope.stride(1), _p(q_pe), spt, sph,
+                              _p(w_uk_t), _p(out), T, H, _stream(stream)))
+    return out
+
+
+def decode(q, kv_cache, block_table, seq_lens, max_seq_len, scale, kv_dtype=KV_BF16, num_splits=0,
+           workspace=None, o_latent=None, o_dtype=DT_F32, lse=None, dev_status=None, stream=None,
+           num_blocks=None):
+    """q [B,Sq,H,576] bf16, kv_cache [num_blocks, 64*row_bytes] uint8 (or a bf16 view), block_table
+    [B,max_blocks] int32, seq_lens [B] int32 -> (o_latent [B,Sq,H,512], lse [B,Sq,H])."""
+    import torch
+    B, Sq, H = q.shape[0], q.shape[1], q.shape[2]
+    dev = q.device
+    if num_blocks is None:
+        num_blocks = kv_cache.numel() * kv_cache.element_size() // (PAGE * row_bytes(kv_dtype))
+    S = resolve_num_splits(num_splits, B, Sq, H, max_seq_len)
+    need = workspace_bytes(B, Sq, H, S)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if o_latent is None:
+        o_latent = torch.empty((B, Sq, H, L), dtype=torch.float32 if o_dtype == DT_F32 else torch.bfloat16,
+                               device=dev)
+    if lse is None:
+        lse = torch.empty((B, Sq, H), dtype=torch.float32, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().mla_decode(_p(q), _p(kv_cache), kv_dtype, int(num_blocks), _p(block_table),
+                            block_table.shape[1], _p(seq_lens), int(max_seq_len), B, Sq, H, float(scale),
+                            int(S), _p(workspace), ws_bytes, _p(o_latent), o_dtype, _p(lse), _p(dev_status),
+                            _stream(stream)))
+    return o_latent, lse
+
+
+def out_proj(o_latent, w_uv, out=None, out_dtype=DT_F32, stream=None):
+    """o_latent [T,H,512] fp32/bf16, W_UV [H,512,128] bf16 -> o [T,H,128]."""
+    import torch
+    T, H = o_latent.shape[0], o_latent.shape[1]
+    in_dtype = DT_F32 if o_latent.dtype == torch.float32 else DT_BF16
+    if out is None:
+        out = torch.empty((T, H, V), dtype=torch.float32 if out_dtype == DT_F32 else torch.bfloat16,
+                          device=o_latent.device)
+    _check(lib().mla_out_proj(_p(o_latent), in_dtype, _p(w_uv), _p(out), out_dtype, T, H, _stream(stream)))
+    return out

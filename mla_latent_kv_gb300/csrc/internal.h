@@ -1,0 +1,61 @@
+// internal.h -- shared declarations of the CUDA library (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mla_latent_kv.h"
+
+namespace mla {
+
+constexpr int kL = MLA_KV_LORA_RANK;  // 512 latent dims (also the V width)
+constexpr int kR = MLA_ROPE_DIM;      // 64 rope dims
+constexpr int kD = MLA_HEAD_DIM;      // 576 = one cached row / one absorbed query
+constexpr int kP = MLA_NOPE_DIM;      // 128
+constexpr int kV = MLA_V_DIM;         // 128
+constexpr int kPage = MLA_PAGE_SIZE;  // 64 tokens per page
+constexpr int kBf16RowBytes = 2 * kD; // 1152
+constexpr int kFp8RowBytes = kD + 8;  // 584
+
+// Everything a decode launch needs, resolved and validated on the host.
+struct DecodeArgs {
+    const uint16_t* q;          // bf16 [B, Sq, H, 576]
+    const uint8_t* cache;       // [num_blocks, 64, row_bytes]
+    int kv_dtype;
+    int64_t num_blocks;
+    const int32_t* block_table; // [B, max_blocks]
+    int max_blocks;
+    const int32_t* seq_lens;    // [B]
+    int max_seq_len;
+    int B, Sq, H;
+    float scale;
+    int num_splits;             // resolved, >= 1
+    float* part_o;              // [B*Sq, S, H, 512] fp32 (num_splits > 1)
+    float* part_lse;            // [B*Sq, S, H]     fp32 (num_splits > 1)
+    void* o_latent;             // [B, Sq, H, 512]
+    int o_dtype;                // mla_dtype
+    float* lse;                 // [B, Sq, H] or null
+    int32_t* dev_status;        // or null
+};
+
+// Token range [j0, j1) of split s of a row with n visible tokens: the row is cut into
+// num_splits page-aligned chunks of round_up(ceil(n / S), 64) tokens; trailing splits may be
+// empty. The same rule is used by every decode kernel.
+__host__ __device__ inline void split_range(int n, int S, int s, int* j0, int* j1) {
+    int per = (n + S - 1) / S;
+    int chunk = ((per + kPage - 1) / kPage) * kPage;
+    int a = s * chunk;
+    int e = a + chunk;
+    *j0 = a < n ? a : n;
+    *j1 = e < n ? e : n;
+}
+
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_absorb_simt(const uint16_t* q_nope, int64_t snt, int64_t snh, const uint16_t* q_pe,
+                               int64_t spt, int64_t sph, const uint16_t* w_uk_t, uint16_t* q_out,
+                               int T, int H, cudaStream_t s);
+cudaError_t launch_out_proj_simt(const void* o_latent, int in_dtype, const uint16_t* w_uv, void* o,
+                                 int out_dtype, int T, int H, cudaStream_t s);
+
+}  // namespace mla

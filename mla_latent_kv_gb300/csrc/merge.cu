@@ -1,0 +1,81 @@
+// merge.cu -- split-KV stage 2: combine the per-split partial states of every (row, head).
+//
+// [vLLM-MLA, Triton MLA section]: stage 1 writes a partial output and LSE per split into an
+// fp32 buffer (B, N, splits, 512 + 1); stage 2 reduces them by LSE. [vLLM-MLA, Prefill
+// section], merge_attn_states: partials are re-weighted by exp(lse - max_lse); an empty partial
+// (o = 0, lse = -inf) has no weight.
+//     M = max_s lse_s,  w_s = exp(lse_s - M),  lse = M + ln sum_s w_s,  o = sum_s w_s o_s / sum_s w_s
+// One warp per (row, head); lane i owns latent dims [16 i, 16 i + 16). The partial states are
+// read once, coalesced (each split's 512 floats are contiguous), and the result written once.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "internal.h"
+
+namespace mla {
+namespace {
+
+constexpr int kWarps = 8;
+
+__global__ void __launch_bounds__(kWarps * 32) merge_kernel(DecodeArgs p) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int64_t item = (int64_t)blockIdx.x * kWarps + warp;  // (row, head)
+    const int64_t n_items = (int64_t)p.B * p.Sq * p.H;
+    if (item >= n_items) return;
+    const int64_t r = item / p.H;
+    const int h = (int)(item % p.H);
+    const int S = p.num_splits;
+    const float* lse_p = p.part_lse + (size_t)r * S * p.H + h;  // stride H between splits
+
+    float M = -CUDART_INF_F;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, lse_p[(size_t)s * p.H]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    float wsum = 0.f;
+    if (M != -CUDART_INF_F) {
+        for (int s = 0; s < S; ++s) {
+            const float ls = lse_p[(size_t)s * p.H];
+            if (ls == -CUDART_INF_F) continue;
+            const float w = __expf(ls - M);
+            wsum += w;
+            const float4* src = reinterpret_cast<const float4*>(
+                p.part_o + (((size_t)r * S + s) * p.H + h) * kL + lane * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float4 v = src[i];
+                acc[4 * i + 0] = fmaf(w, v.x, acc[4 * i + 0]);
+                acc[4 * i + 1] = fmaf(w, v.y, acc[4 * i + 1]);
+                acc[4 * i + 2] = fmaf(w, v.z, acc[4 * i + 2]);
+                acc[4 * i + 3] = fmaf(w, v.w, acc[4 * i + 3]);
+            }
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const size_t base = ((size_t)r * p.H + h) * kL + lane * 16;
+    if (p.o_dtype == MLA_DT_F32) {
+        float4* dst = reinterpret_cast<float4*>((float*)p.o_latent + base);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            dst[i] = make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
+    } else {
+        __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>((__nv_bfloat16*)p.o_latent + base);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+    }
+    if (lane == 0 && p.lse) p.lse[(size_t)r * p.H + h] = wsum > 0.f ? M + __logf(wsum) : -CUDART_INF_F;
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
+    const int64_t n_items = (int64_t)a.B * a.Sq * a.H;
+    const int64_t blocks = (n_items + kWarps - 1) / kWarps;
+    merge_kernel<<<(unsigned)blocks, kWarps * 32, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace mla

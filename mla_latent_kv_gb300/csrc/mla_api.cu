@@ -1,0 +1,229 @@
+// mla_api.cu -- the extern "C" boundary: host-side validation, split planning and launches.
+//
+// Nothing here allocates, frees or synchronises: every call validates its arguments, resolves
+// the split plan from host-known quantities only (the pages' "no sync" rule for metadata,
+// [vLLM-MLA, metadata section]: host upper bounds instead of device lengths) and enqueues
+// kernels on the caller's stream.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "internal.h"
+
+namespace {
+
+thread_local char g_detail[512] = "";
+
+mla_status fail(mla_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_detail, sizeof g_detail, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+mla_status ok() {
+    g_detail[0] = '\0';
+    return MLA_OK;
+}
+
+mla_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(MLA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return sms;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(mla_status s) {
+    switch (s) {
+        case MLA_OK: return "MLA_OK";
+        case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+        case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+        case MLA_ERR_WORKSPACE_TOO_SMALL: return "MLA_ERR_WORKSPACE_TOO_SMALL";
+        case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    }
+    return "MLA_ERR_UNKNOWN";
+}
+
+const char* mla_last_error_detail(void) { return g_detail; }
+
+int64_t mla_kv_row_bytes(mla_kv_dtype kv_dtype) {
+    switch (kv_dtype) {
+        case MLA_KV_BF16: return mla::kBf16RowBytes;
+        case MLA_KV_FP8_E4M3_SCALED: return mla::kFp8RowBytes;
+    }
+    return -1;
+}
+
+int mla_default_num_splits(int max_seq_len, int sm_count) {
+    if (max_seq_len < 0 || sm_count < 1) return -1;
+    int ideal = std::max(1, max_seq_len / 512);
+    int p2 = 1;
+    while (p2 < ideal) p2 *= 2;
+    return std::min(p2, 2 * sm_count);
+}
+
+int mla_resolve_num_splits(int num_splits, int B, int Sq, int H, int max_seq_len) {
+    if (num_splits > 0) return num_splits;
+    if (num_splits < -1 || B < 0 || Sq < 1 || H < 1 || max_seq_len < 0) return -1;
+    int sms = device_sm_count();
+    if (sms < 1) return -1;
+    if (num_splits == 0) return mla_default_num_splits(max_seq_len, sms);
+    // GB300 plan: each unit (one query row x one split) occupies one pair of SMs. Estimate the
+    // time of S splits as  waves(S) * pages_per_split(S) * t_page  plus the partial-state
+    // traffic of the split path, and take the cheapest S.
+    const int slots = std::max(1, sms / 2);
+    const int64_t rows = (int64_t)B * Sq;
+    const int pages = std::max(1, (max_seq_len + mla::kPage - 1) / mla::kPage);
+    if (rows == 0) return 1;
+    const double page_bytes = (double)mla::kPage * mla::kBf16RowBytes;
+    const double partial_bytes_per_unit = (double)H * (mla::kL + 1) * 4.0 * 2.0;  // write + read
+    double best = 1e300;
+    int best_s = 1;
+    for (int S = 1; S <= pages; ++S) {
+        int64_t units = rows * S;
+        int64_t waves = (units + slots - 1) / slots;
+        int per = (pages + S - 1) / S;
+        double t = (double)waves * per * page_bytes * slots;  // bytes moved at the wave rate
+        if (S > 1) t += (double)units * partial_bytes_per_unit;
+        if (t < best * 0.999) {
+            best = t;
+            best_s = S;
+        }
+    }
+    return best_s;
+}
+
+size_t mla_decode_workspace_bytes(int B, int Sq, int H, int num_splits) {
+    if (B <= 0 || Sq <= 0 || H <= 0 || num_splits <= 1) return 0;
+    size_t units = (size_t)B * Sq * num_splits * H;
+    size_t o_bytes = units * mla::kL * sizeof(float);
+    size_t lse_bytes = units * sizeof(float);
+    size_t total = ((o_bytes + 255) / 256) * 256 + ((lse_bytes + 255) / 256) * 256;
+    return total;
+}
+
+mla_status mla_absorb_q(const void* q_nope, int64_t snt, int64_t snh, const void* q_pe, int64_t spt,
+                        int64_t sph, const void* W_UK_T, void* q_out, int T, int H, mla_stream_t stream) {
+    if (T < 0) return fail(MLA_ERR_INVALID_ARG, "mla_absorb_q: T=%d < 0", T);
+    if (H < 1 || H > MLA_MAX_HEADS)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_absorb_q: H=%d outside [1, %d]", H, MLA_MAX_HEADS);
+    if (T == 0) return ok();
+    if (!q_nope || !W_UK_T || !q_out) return fail(MLA_ERR_INVALID_ARG, "mla_absorb_q: null pointer");
+    if (!aligned16(q_nope) || !aligned16(W_UK_T) || !aligned16(q_out) || (q_pe && !aligned16(q_pe)))
+        return fail(MLA_ERR_UNSUPPORTED, "mla_absorb_q: pointers must be 16-byte aligned");
+    if (snt < 0 || snh < 0 || snt % 8 || snh % 8 || (q_pe && (spt < 0 || sph < 0 || spt % 8 || sph % 8)))
+        return fail(MLA_ERR_UNSUPPORTED, "mla_absorb_q: strides must be non-negative multiples of 8");
+    if (snh < mla::kP && H > 1)
+        return fail(MLA_ERR_INVALID_ARG, "mla_absorb_q: q_nope head stride %lld < 128", (long long)snh);
+    cudaError_t e = mla::launch_absorb_simt((const uint16_t*)q_nope, snt, snh, (const uint16_t*)q_pe, spt,
+                                           sph, (const uint16_t*)W_UK_T, (uint16_t*)q_out, T, H,
+                                           (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "mla_absorb_q launch");
+    return ok();
+}
+
+mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype, int64_t num_blocks,
+                      const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int max_seq_len,
+                      int B, int Sq, int H, float scale, int num_splits, void* workspace,
+                      size_t workspace_bytes, void* o_latent, mla_dtype o_dtype, float* lse,
+                      int32_t* dev_status, mla_stream_t stream) {
+    if (B < 0) return fail(MLA_ERR_INVALID_ARG, "mla_decode: B=%d < 0", B);
+    if (Sq < 1) return fail(MLA_ERR_INVALID_ARG, "mla_decode: Sq=%d < 1", Sq);
+    if (H < 1 || H > MLA_MAX_HEADS)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: H=%d outside [1, %d]", H, MLA_MAX_HEADS);
+    if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3_SCALED)
+        return fail(MLA_ERR_INVALID_ARG, "mla_decode: unknown kv_dtype %d", (int)kv_dtype);
+    if (o_dtype != MLA_DT_F32 && o_dtype != MLA_DT_BF16)
+        return fail(MLA_ERR_INVALID_ARG, "mla_decode: unknown o_dtype %d", (int)o_dtype);
+    if (max_seq_len < 0 || max_blocks < 0 || num_blocks < 0)
+        return fail(MLA_ERR_INVALID_ARG, "mla_decode: negative max_seq_len/max_blocks/num_blocks");
+    if ((int64_t)max_seq_len > (int64_t)max_blocks * mla::kPage)
+        return fail(MLA_ERR_INVALID_ARG, "mla_decode: max_seq_len=%d exceeds max_blocks*64=%lld", max_seq_len,
+                    (long long)max_blocks * mla::kPage);
+    if (!(std::isfinite(scale)) || scale <= 0.f)
+        return fail(MLA_ERR_INVALID_ARG, "mla_decode: scale must be finite and > 0");
+    if (num_splits < -1) return fail(MLA_ERR_INVALID_ARG, "mla_decode: num_splits=%d < -1", num_splits);
+    if (B == 0) return ok();
+    if (!q || !o_latent || !seq_lens || (max_seq_len > 0 && (!kv_cache || !block_table)))
+        return fail(MLA_ERR_INVALID_ARG, "mla_decode: null pointer");
+    if (!aligned16(q) || (kv_cache && !aligned16(kv_cache)) || !aligned16(o_latent))
+        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: q, kv_cache and o_latent must be 16-byte aligned");
+    if (kv_dtype == MLA_KV_FP8_E4M3_SCALED)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: FP8 cache not available in this build");
+    int S = mla_resolve_num_splits(num_splits, B, Sq, H, max_seq_len);
+    if (S < 1) return fail(MLA_ERR_CUDA, "mla_decode: could not resolve num_splits (no CUDA device?)");
+    size_t need = mla_decode_workspace_bytes(B, Sq, H, S);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+        return fail(MLA_ERR_WORKSPACE_TOO_SMALL, "mla_decode: workspace %zu bytes < %zu needed for %d splits",
+                    workspace ? workspace_bytes : (size_t)0, need, S);
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: workspace must be 256-byte aligned");
+
+    mla::DecodeArgs a{};
+    a.q = (const uint16_t*)q;
+    a.cache = (const uint8_t*)kv_cache;
+    a.kv_dtype = kv_dtype;
+    a.num_blocks = num_blocks;
+    a.block_table = block_table;
+    a.max_blocks = max_blocks;
+    a.seq_lens = seq_lens;
+    a.max_seq_len = max_seq_len;
+    a.B = B;
+    a.Sq = Sq;
+    a.H = H;
+    a.scale = scale;
+    a.num_splits = S;
+    if (S > 1) {
+        size_t units = (size_t)B * Sq * S * H;
+        size_t o_bytes = ((units * mla::kL * sizeof(float) + 255) / 256) * 256;
+        a.part_o = (float*)workspace;
+        a.part_lse = (float*)((char*)workspace + o_bytes);
+    }
+    a.o_latent = o_latent;
+    a.o_dtype = o_dtype;
+    a.lse = lse;
+    a.dev_status = dev_status;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = mla::launch_decode_simt(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
+    if (S > 1) {
+        e = mla::launch_merge(a, st);
+        if (e != cudaSuccess) return cuda_fail(e, "mla_decode merge launch");
+    }
+    return ok();
+}
+
+mla_status mla_out_proj(const void* o_latent, mla_dtype in_dtype, const void* W_UV, void* o, mla_dtype out_dtype,
+                        int T, int H, mla_stream_t stream) {
+    if (T < 0) return fail(MLA_ERR_INVALID_ARG, "mla_out_proj: T=%d < 0", T);
+    if (H < 1 || H > MLA_MAX_HEADS)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_out_proj: H=%d outside [1, %d]", H, MLA_MAX_HEADS);
+    if ((in_dtype != MLA_DT_F32 && in_dtype != MLA_DT_BF16) || (out_dtype != MLA_DT_F32 && out_dtype != MLA_DT_BF16))
+        return fail(MLA_ERR_INVALID_ARG, "mla_out_proj: unknown dtype");
+    if (T == 0) return ok();
+    if (!o_latent || !W_UV || !o) return fail(MLA_ERR_INVALID_ARG, "mla_out_proj: null pointer");
+    if (!aligned16(o_latent) || !aligned16(W_UV) || !aligned16(o))
+        return fail(MLA_ERR_UNSUPPORTED, "mla_out_proj: pointers must be 16-byte aligned");
+    cudaError_t e = mla::launch_out_proj_simt(o_latent, in_dtype, (const uint16_t*)W_UV, o, out_dtype, T, H,
+                                              (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "mla_out_proj launch");
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+"""GPU parity of mla_decode (and its split-KV merge) against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import mla_inputs as mi
+import oracle
+from parity_util import compare_decode, run_decode, torch_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle(c, sel=None):
+    return oracle.decode_absorbed(c["q"], c["cache"], c["kv"], c["num_blocks"], c["block_table"],
+                                  c["seq_lens"], c["B"], c["Sq"], c["H"], c["scale"], sel=sel)
+
+
+@pytest.mark.parametrize("num_splits", [1, 2, 3, 0, -1])
+def test_tiny_workload(num_splits):
+    c = mi.workload_case("tiny")
+    o, lse, st = run_decode(c, num_splits)
+    o_ref, lse_ref = _oracle(c)
+    assert st == 0
+    compare_decode(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("num_splits", [1, 4, 7, 0])
+def test_ragged_multi_page(num_splits):
+    """Several pages, ragged tails (1, 63, 64, 65 tokens...), poisoned unused rows."""
+    c = mi.decode_case(6, 1, 128, [1, 63, 64, 65, 700, 1000], seed=20)
+    o, lse, st = run_decode(c, num_splits)
+    o_ref, lse_ref = _oracle(c)
+    assert st == 0
+    compare_decode(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("H", [1, 20, 100])
+def test_head_counts(H):
+    c = mi.decode_case(2, 1, H, [130, 7], seed=21)
+    o, lse, st = run_decode(c, 2)
+    o_ref, lse_ref = _oracle(c)
+    assert st == 0
+    compare_decode(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("num_splits", [1, 3])
+def test_causal_two_row_queries_and_empty_rows(num_splits):
+    """Sq = 2: row t sees seq_len - (1 - t) tokens; seq_len 0 and 1 give empty rows."""
+    c = mi.decode_case(4, 2, 32, [0, 1, 2, 200], seed=22)
+    o, lse, st = run_decode(c, num_splits)
+    o_ref, lse_ref = _oracle(c)
+    assert st == 0
+    assert np.all(lse_ref[0] == -np.inf) and lse_ref[1, 0, 0] == -np.inf
+    compare_decode(o, lse, o_ref, lse_ref)
+
+
+def test_bf16_output():
+    c = mi.decode_case(3, 1, 64, [5, 64, 300], seed=23)
+    o, lse, st = run_decode(c, 2, o_dtype=1)
+    o_ref, lse_ref = _oracle(c)
+    # one bf16 rounding of the output adds up to half an ulp of |o|
+    compare_decode(o, lse, o_ref, lse_ref, extra_abs=float(np.abs(o_ref).max()) * 2.0 ** -9)
+
+
+def test_bad_block_id_sets_device_status():
+    c = mi.decode_case(2, 1, 16, [100, 100], seed=24)
+    bt = c["block_table"].copy()
+    bt[1, 1] = c["num_blocks"] + 5  # needed entry out of range
+    c2 = dict(c, block_table=bt)
+    _, _, st = run_decode(c2, 1)
+    assert st & 0x1
+    _, _, st_ok = run_decode(c, 1)
+    assert st_ok == 0
+
+
+def test_batch_zero_and_workspace_checks():
+    import torch
+    import mla_latent_kv_gb300 as mla
+    c = mi.decode_case(2, 1, 16, [100, 300], seed=25)
+    d = torch_dev(c)
+    q0 = d["q"][:0]
+    o, lse = mla.decode(q0, d["cache"], d["block_table"][:0], d["seq_lens"][:0], 0, c["scale"], num_splits=1)
+    assert o.shape[0] == 0
+    with pytest.raises(mla.MlaError) as e:
+        mla.decode(d["q"], d["cache"], d["block_table"], d["seq_lens"], 300, c["scale"], num_splits=4,
+                   workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == mla.ERR_WORKSPACE_TOO_SMALL
+
+
+# ----------------------------------------------------------------------------- full workloads
+def _sampled(c, heads=(0, 37, 127)):
+    sel = [(b, t, h) for b in range(c["B"]) for t in range(c["Sq"]) for h in heads if h < c["H"]]
+    return np.array(sel, np.int32)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,num_splits", [("dsv3", -1), ("dsv3", 0), ("ragged", -1), ("long_mtp", 0),
+                                             ("long_mtp", -1)])
+def test_full_workload_sampled(name, num_splits):
+    c = mi.workload_case(name)
+    o, lse, st = run_decode(c, num_splits)
+    assert st == 0
+    sel = _sampled(c)
+    o_ref, lse_ref = _oracle(c, sel)
+    idx = (sel[:, 0] * c["Sq"] + sel[:, 1]) * c["H"] + sel[:, 2]
+    compare_decode(o.reshape(-1, 512)[idx], lse.reshape(-1)[idx], o_ref, lse_ref)
+    # every row of the full output: finite, lse finite exactly where the row has tokens
+    n = np.array([[oracle.row_len(int(s), c["Sq"], t) for t in range(c["Sq"])] for s in c["seq_lens"]])
+    assert np.isfinite(o).all()
+    assert np.array_equal(np.isfinite(lse), np.broadcast_to((n > 0)[..., None], lse.shape))

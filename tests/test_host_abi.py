@@ -1,0 +1,103 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every function the
+header declares, and its host-only helpers and argument validation behave as documented."""
+import ctypes
+
+import pytest
+
+import mla_inputs as mi
+import oracle
+
+mla = pytest.importorskip("mla_latent_kv_gb300")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mla_latent_kv_gb300 import build
+    build.build()
+    return mla.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = mla.declared_functions()
+    assert {"mla_absorb_q", "mla_decode", "mla_out_proj"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/mla_latent_kv.h but not exported"
+
+
+def test_status_strings_and_row_bytes(lib):
+    assert mla.status_string(0) == "MLA_OK"
+    assert mla.status_string(3) == "MLA_ERR_WORKSPACE_TOO_SMALL"
+    assert mla.status_string(99) == "MLA_ERR_UNKNOWN"
+    assert mla.row_bytes(mla.KV_BF16) == 1152 == oracle.row_bytes(oracle.KV_BF16)
+    assert mla.row_bytes(mla.KV_FP8) == 584 == oracle.row_bytes(oracle.KV_FP8)
+    assert mla.row_bytes(7) == -1
+
+
+def test_default_num_splits_agrees_with_oracle(lib):
+    for n in [0, 1, 511, 512, 513, 1024, 4096, 8192, 32768, 131072, 10 ** 6]:
+        for sms in [1, 76, 148, 152]:
+            assert mla.default_num_splits(n, sms) == oracle.default_num_splits(n, sms), (n, sms)
+    assert mla.default_num_splits(-1, 152) == -1 and mla.default_num_splits(10, 0) == -1
+
+
+def test_workspace_bytes(lib):
+    assert mla.workspace_bytes(64, 1, 128, 1) == 0
+    ws = mla.workspace_bytes(4, 2, 128, 256)
+    units = 4 * 2 * 256 * 128
+    assert ws >= units * 513 * 4 and ws % 256 == 0 and ws - units * 513 * 4 < 512
+
+
+def test_forced_split_count_needs_no_device(lib):
+    assert lib.mla_resolve_num_splits(5, 2, 1, 16, 300) == 5
+    assert lib.mla_resolve_num_splits(-2, 2, 1, 16, 300) == -1
+
+
+def _decode_call(lib, **kw):
+    args = dict(q=None, kv_cache=None, kv_dtype=0, num_blocks=0, block_table=None, max_blocks=0,
+                seq_lens=None, max_seq_len=0, B=1, Sq=1, H=16, scale=0.07, num_splits=1, workspace=None,
+                workspace_bytes=0, o_latent=None, o_dtype=0, lse=None, dev_status=None, stream=None)
+    args.update(kw)
+    return lib.mla_decode(*args.values())
+
+
+def test_decode_validation_before_any_launch(lib):
+    assert _decode_call(lib, H=0) == mla.ERR_UNSUPPORTED
+    assert _decode_call(lib, H=129) == mla.ERR_UNSUPPORTED
+    assert _decode_call(lib, B=-1) == mla.ERR_INVALID_ARG
+    assert _decode_call(lib, Sq=0) == mla.ERR_INVALID_ARG
+    assert _decode_call(lib, kv_dtype=5) == mla.ERR_INVALID_ARG
+    assert _decode_call(lib, o_dtype=9) == mla.ERR_INVALID_ARG
+    assert _decode_call(lib, scale=0.0) == mla.ERR_INVALID_ARG
+    assert _decode_call(lib, scale=float("nan")) == mla.ERR_INVALID_ARG
+    assert _decode_call(lib, max_seq_len=65, max_blocks=1) == mla.ERR_INVALID_ARG
+    assert _decode_call(lib, num_splits=-3) == mla.ERR_INVALID_ARG
+    assert _decode_call(lib) == mla.ERR_INVALID_ARG  # null q / o_latent
+    assert b"null" in lib.mla_last_error_detail()
+    assert _decode_call(lib, B=0) == mla.OK  # nothing to do, nothing launched
+    bad = ctypes.c_void_p(0x1001)  # misaligned; rejected before any device access
+    assert _decode_call(lib, q=bad, o_latent=bad, seq_lens=bad) == mla.ERR_UNSUPPORTED
+
+
+def test_gemm_validation_before_any_launch(lib):
+    f = lib.mla_absorb_q
+    assert f(None, 128, 128, None, 64, 64, None, None, 4, 0, None) == mla.ERR_UNSUPPORTED
+    assert f(None, 128, 128, None, 64, 64, None, None, -1, 4, None) == mla.ERR_INVALID_ARG
+    assert f(None, 128, 128, None, 64, 64, None, None, 0, 4, None) == mla.OK
+    assert f(None, 128, 128, None, 64, 64, None, None, 3, 4, None) == mla.ERR_INVALID_ARG
+    al = ctypes.c_void_p(0x1000)
+    assert f(al, 100, 128, None, 64, 64, al, al, 3, 4, None) == mla.ERR_UNSUPPORTED  # stride % 8
+    g = lib.mla_out_proj
+    assert g(None, 0, None, None, 0, 4, 200, None) == mla.ERR_UNSUPPORTED
+    assert g(None, 7, None, None, 0, 4, 2, None) == mla.ERR_INVALID_ARG
+    assert g(None, 0, None, None, 0, 0, 2, None) == mla.OK
+    assert g(None, 0, None, None, 0, 4, 2, None) == mla.ERR_INVALID_ARG
+
+
+def test_workload_table_matches_configs():
+    w = mi.WORKLOADS
+    assert (w["dsv3"]["B"], w["dsv3"]["H"], w["dsv3"]["lens"][0]) == (64, 128, 4096)
+    assert (w["long_mtp"]["B"], w["long_mtp"]["Sq"], w["long_mtp"]["lens"][0]) == (4, 2, 131072)
+    assert w["fp8"]["kv"] == mi.KV_FP8 and w["fp8"]["lens"][0] == 8192
+    import numpy as np
+    lens = mi.draw_lengths("loguniform", 128, np.random.default_rng(2))
+    assert list(lens[:6]) == [1, 63, 64, 65, 128, 32768] and lens.min() >= 1 and lens.max() <= 32768
