@@ -90,7 +90,7 @@ def test_end_to_end_vs_nonabsorbed(B, Sq, H, lens, splits):
     o_ref, ol_ref, lse_ref = oracle.decode_nonabsorbed(c["q_nope"], c["q_pe"], c["cache"], c["kv"],
                                                        c["num_blocks"], c["block_table"], c["seq_lens"],
                                                        c["w_uk_t"], c["w_uv"], B, Sq, H, c["scale"])
-    ol_g, lse_g, o_g = to_f64(ol), to_f64(lse), to_f64(o)
+    ol_g, lse_g, o_g = to_f64(ol), to_f64(lse), to_f64(o).reshape(o_ref.shape)
     fin = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(lse_g), fin)
     assert np.abs(ol_g - ol_ref).max() <= TOL_MAX_ABS and rel_l2(ol_g[fin], ol_ref[fin]) <= TOL_REL_L2
