@@ -51,6 +51,7 @@ __host__ __device__ inline void split_range(int n, int S, int s, int* j0, int* j
 }
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_absorb_simt(const uint16_t* q_nope, int64_t snt, int64_t snh, const uint16_t* q_pe,
                                int64_t spt, int64_t sph, const uint16_t* w_uk_t, uint16_t* q_out,

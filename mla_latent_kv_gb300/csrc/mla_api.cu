@@ -166,8 +166,13 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: q, kv_cache and o_latent must be 16-byte aligned");
     if (kv_dtype == MLA_KV_FP8_E4M3_SCALED)
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: FP8 cache not available in this build");
+    if (num_blocks > (int64_t)(INT32_MAX / mla::kPage))
+        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: num_blocks=%lld too large (max %d)", (long long)num_blocks,
+                    INT32_MAX / mla::kPage);
     int S = mla_resolve_num_splits(num_splits, B, Sq, H, max_seq_len);
     if (S < 1) return fail(MLA_ERR_CUDA, "mla_decode: could not resolve num_splits (no CUDA device?)");
+    if ((int64_t)B * Sq * S > (int64_t)1 << 30)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: B*Sq*num_splits=%lld too large", (long long)B * Sq * S);
     size_t need = mla_decode_workspace_bytes(B, Sq, H, S);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need))
         return fail(MLA_ERR_WORKSPACE_TOO_SMALL, "mla_decode: workspace %zu bytes < %zu needed for %d splits",
@@ -200,7 +205,7 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
     a.lse = lse;
     a.dev_status = dev_status;
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = mla::launch_decode_simt(a, st);
+    cudaError_t e = mla::launch_decode_sm103(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
     if (S > 1) {
         e = mla::launch_merge(a, st);
