@@ -77,7 +77,8 @@ constexpr int OFF_ABORT = 260;
 constexpr int OFF_FLAGS = 272;   // u32 [2][4]: per P buffer, per softmax warp "some row rescaled"
 constexpr int OFF_ALPHA = 512;   // f32 [2][128]: per P buffer, per head rescale factor
 constexpr int OFF_STAT_M = 1536; // f32 [128]: final running max (log2 domain)
-constexpr int OFF_STAT_L = 2048; // f32 [128]: final row sum
+constexpr int OFF_STAT_L = 2048; // f32 [128]: final row sum of the bf16-rounded P (normalises O)
+constexpr int OFF_STAT_LT = 2560; // f32 [128]: final row sum of the unrounded P (gives the LSE)
 constexpr int OFF_DATA = kCtrlBytes;
 constexpr int OFF_P = OFF_DATA + kStages * kVStageBytes;  // CTA1 only
 
@@ -240,7 +241,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 bar_arrive(bar(B_QREADY));
             }
             const float sl2 = p.scale * 1.4426950408889634f;
-            float m_run = -CUDART_INF_F, l_run = 0.f;
+            // l_run sums P exactly as the PV MMA sees it (bf16), so that o = P V / l_run is
+            // consistent even when one token dominates; lt_run sums the unrounded fp32 P for lse.
+            float m_run = -CUDART_INF_F, l_run = 0.f, lt_run = 0.f;
             const uint32_t p_remote = map_to_rank(sbase + OFF_P, 1);
             const uint32_t alpha_remote = map_to_rank(sbase + OFF_ALPHA, 1);
             const uint32_t flags_remote = map_to_rank(sbase + OFF_FLAGS, 1);
@@ -271,16 +274,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     m_run = mt;
                 }
                 uint32_t pk[32];
-                float sum = 0.f;
+                float sum = 0.f, sum_t = 0.f;
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    pk[c] = pack_bf16x2(exp2f(__uint_as_float(s0[2 * c]) - m_run),
-                                        exp2f(__uint_as_float(s0[2 * c + 1]) - m_run));
-                    pk[16 + c] = pack_bf16x2(exp2f(__uint_as_float(s1[2 * c]) - m_run),
-                                             exp2f(__uint_as_float(s1[2 * c + 1]) - m_run));
+                    const float a0 = exp2f(__uint_as_float(s0[2 * c]) - m_run);
+                    const float a1 = exp2f(__uint_as_float(s0[2 * c + 1]) - m_run);
+                    const float b0 = exp2f(__uint_as_float(s1[2 * c]) - m_run);
+                    const float b1 = exp2f(__uint_as_float(s1[2 * c + 1]) - m_run);
+                    pk[c] = pack_bf16x2(a0, a1);
+                    pk[16 + c] = pack_bf16x2(b0, b1);
+                    sum_t += (a0 + a1) + (b0 + b1);
                     sum += bf16_lo_f(pk[c]) + bf16_hi_f(pk[c]) + bf16_lo_f(pk[16 + c]) + bf16_hi_f(pk[16 + c]);
                 }
                 l_run = l_run * alpha + sum;
+                lt_run = lt_run * alpha + sum_t;
                 if (u > 0 && !warp_wait<true>(bar(B_PEMPTY + sb), (u - 1) & 1, abort, ds)) break;
                 const uint32_t pdst = p_remote + sb * kPBytes + row * 128;
 #pragma unroll
@@ -295,6 +302,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             st_cluster_u32(map_to_rank(sbase + OFF_STAT_M, 1) + 4u * row, __float_as_uint(m_run));
             st_cluster_u32(map_to_rank(sbase + OFF_STAT_L, 1) + 4u * row, __float_as_uint(l_run));
+            st_cluster_u32(map_to_rank(sbase + OFF_STAT_LT, 1) + 4u * row, __float_as_uint(lt_run));
             bar_arrive_remote(bar(B_STATS), 1);
             // no multicast commit may still be on its way to this CTA when it exits
             volatile int dummy = 0;
@@ -402,9 +410,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float m = reinterpret_cast<volatile float*>(smem + OFF_STAT_M)[row];
             const float l = reinterpret_cast<volatile float*>(smem + OFF_STAT_L)[row];
+            const float lt = reinterpret_cast<volatile float*>(smem + OFF_STAT_LT)[row];
             const bool empty = !(l > 0.f) || npages == 0;
             const float inv = empty ? 0.f : 1.f / l;
-            const float lse_v = empty ? -CUDART_INF_F : (m + log2f(l)) * 0.6931471805599453f;
+            const float lse_v = empty ? -CUDART_INF_F : (m + log2f(lt)) * 0.6931471805599453f;
             const bool live = row < p.H;
             const bool split = p.num_splits > 1;
             float* of = nullptr;
