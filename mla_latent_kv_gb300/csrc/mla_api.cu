@@ -171,6 +171,8 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
                     INT32_MAX / mla::kPage);
     int S = mla_resolve_num_splits(num_splits, B, Sq, H, max_seq_len);
     if (S < 1) return fail(MLA_ERR_CUDA, "mla_decode: could not resolve num_splits (no CUDA device?)");
+    if ((int64_t)B * Sq * H > (int64_t)INT32_MAX)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: B*Sq*H=%lld too large", (long long)B * Sq * H);
     if ((int64_t)B * Sq * S > (int64_t)1 << 30)
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: B*Sq*num_splits=%lld too large", (long long)B * Sq * S);
     size_t need = mla_decode_workspace_bytes(B, Sq, H, S);
