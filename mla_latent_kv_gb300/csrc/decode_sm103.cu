@@ -5,26 +5,32 @@
 // row's visible tokens [j0, j1) (one split of it), every head reading the same 576-element
 // cached row:  S = scale * Q K^T,  P = softmax(S),  O = P V  with V = the first 512 dims.
 //
-// Design (one thread-block cluster of two CTAs per (query row, split) unit):
-//   CTA 0 ("scores")  loads Q (128 heads x 576 bf16) once by TMA and keeps it resident in tensor
-//                     memory, streams the row's 64-token pages through a 3-stage TMA ring (9
-//                     panels of 64 dims, 128-byte swizzle), computes S = Q K^T per page with
-//                     tcgen05.mma (M=128 heads, N=64 tokens, K=576, A from TMEM) into a
-//                     double-buffered TMEM accumulator, and runs the fp32 online softmax (one
-//                     thread per head). It writes P (bf16, already in the MMA's swizzled K-major
-//                     layout) straight into CTA 1's shared memory (4 buffers deep), with the
-//                     per-head rescale factors, and releases each buffer with one cluster-scope
-//                     arrive.
+// One thread-block cluster of two CTAs per (query row, split) unit; pages are taken two at a
+// time ("groups" of 128 tokens) so that every tensor-core instruction has N >= 128, the shape
+// at which tcgen05.mma runs at its full rate.
+//
+//   CTA 0 ("scores")  Q: the 512 latent dims (128 heads x 512 bf16) are loaded once by TMA and
+//                     kept in tensor memory; the 64 rope dims stay in shared memory.
+//                     K: the group's two pages stream through a ring of nine 16 KB slots, one
+//                     slot per 64-dim panel holding both pages' rows (128 rows, 128-byte
+//                     swizzle), refilled panel by panel as the MMAs release them, with the pages
+//                     further ahead prefetched into L2.
+//                     S = Q K^T per group: 36 tcgen05.mma of M=128 heads x N=128 tokens x K=16
+//                     (32 with A from TMEM, 4 with A = rope dims from shared memory) into one of
+//                     two 128-column TMEM buffers.
+//                     Softmax: eight warps, two per TMEM lane quarter, each owning one page of
+//                     the group for 32 heads; fp32 online softmax with a lazily moved running
+//                     max (rescale only when a row's max grows by more than 2^8). P (bf16, in
+//                     the MMA's swizzled K-major layout) and the per-head rescale factors are
+//                     written to a local staging buffer and sent to CTA 1 with one bulk
+//                     shared-to-shared copy per page (counted by bytes on CTA 1's barrier).
 //   CTA 1 ("output")  holds the 128 x 512 fp32 output accumulator -- all 512 TMEM columns of its
-//                     SM, which is why the work is split over two SMs -- streams the same pages'
-//                     first 512 dims (mostly L2 hits, 2-stage ring), and accumulates O += P V with
-//                     tcgen05.mma (M=128, N=2x256, K=64, V read as an MN-major operand straight
-//                     from the TMA tile). Its four other warps only act on request: rescale O,
-//                     zero the V rows past the end of the last page, and the epilogue.
-// Neither CTA repeats the other's tensor-core work: per page the pair issues exactly the
-// algorithm's 2*128*64*(576+512) flops. The softmax rescales O lazily: the running max only moves
-// (and O is rescaled) when a row's max grows by more than 2^8, which keeps every exp2 argument
-// <= 8 and makes rescaling rare after the first page.
+//                     SM, the reason the work is split over two SMs -- streams the pages'
+//                     first 512 dims (mostly L2 hits), and accumulates O += P V per page with
+//                     tcgen05.mma (M=128, N=2x256, K=64; V read as an MN-major operand straight
+//                     from the TMA tile). Four helper warps act on request: rescale O, zero the
+//                     V rows past the end of the last page, and the epilogue.
+// Per page the pair issues exactly the algorithm's 2*128*64*(576+512) flops.
 //
 // Rows past the split's last visible token are masked by index (S = -inf) and, in the last
 // partial page, zeroed in CTA 1's V tile so that stale or NaN bytes cannot leak through 0 * NaN.
@@ -48,63 +54,70 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax / correction+epilogue
-constexpr int kKStages = 3;    // CTA 0 ring of full pages (K = all 576 dims)
-constexpr int kVStages = 2;    // CTA 1 ring of V (first 512 dims)
-constexpr int kPBufs = 4;      // P buffers in CTA 1
-constexpr int kPanelBytes = 64 * 128;          // 64 rows x 64 bf16 (one 128-byte swizzle span)
-constexpr int kKStageBytes = 9 * kPanelBytes;  // 73,728
-constexpr int kVStageBytes = 8 * kPanelBytes;  // 65,536
-constexpr int kQPanelBytes = 128 * 128;        // 128 heads x 64 dims of Q
-constexpr int kPBytes = 128 * 128;             // P: 128 heads x 64 tokens
+constexpr int kThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (CTA 0) / 2-5 helpers (CTA 1)
+constexpr int kSlots = 9;            // CTA 0 K ring: one slot = one 64-dim panel of a 2-page group
+constexpr int kSlotBytes = 128 * 128;
+constexpr int kPageBox = 64 * 128;   // one page's rows of one panel
+constexpr int kPrefetchGroups = 3;   // groups prefetched into L2 ahead of the ring
+constexpr int kStageBufs = 3;        // CTA 0 P staging buffers (one page each)
+constexpr int kPBufs = 4;            // CTA 1 P buffers (one page each)
+constexpr int kVStages = 2;          // CTA 1 V ring (one page each)
+constexpr int kVStageBytes = 8 * kPageBox;  // 65,536
+constexpr int kPBytes = 128 * 128;          // P page: 128 heads x 64 tokens bf16
+constexpr int kPMsgBytes = kPBytes + 512 + 16;  // P + alpha[128] + flag word: one bulk copy
+constexpr int kPBufStride = 17 * 1024;
 constexpr int kCtrlBytes = 4096;
-constexpr int kSmem0 = kCtrlBytes + kKStages * kKStageBytes;                     // 225,280
-constexpr int kSmem1 = kCtrlBytes + kVStages * kVStageBytes + kPBufs * kPBytes;  // 200,704
+// CTA 0 layout
+constexpr int OFF_QROPE = kCtrlBytes;                      // 16 KB: Q rope panel
+constexpr int OFF_RING = OFF_QROPE + kSlotBytes;           // 9 x 16 KB
+constexpr int OFF_STAGE = OFF_RING + kSlots * kSlotBytes;  // 3 x 17 KB
+constexpr int kSmem0 = OFF_STAGE + kStageBufs * kPBufStride;
+// CTA 1 layout
+constexpr int OFF_V = kCtrlBytes;
+constexpr int OFF_PB = OFF_V + kVStages * kVStageBytes;
+constexpr int kSmem1 = OFF_PB + kPBufs * kPBufStride;
 constexpr int kSmemBytes = kSmem0 > kSmem1 ? kSmem0 : kSmem1;
 static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
-static_assert(9 * kQPanelBytes <= 2 * kKStageBytes, "Q is staged in the first two K stages");
+static_assert(kPMsgBytes % 16 == 0 && kPMsgBytes <= kPBufStride, "P message");
 
-// Barrier slots (8 bytes each). Both CTAs use one layout so that a multicast commit from CTA 1
-// lands on CTA 0's B_PEMPTY slot.
+// Barrier slots (8 bytes each) at the start of the control block; one layout for both CTAs so
+// that a multicast commit from CTA 1 lands on CTA 0's B_PEMPTY slots.
 enum : int {
-    B_KFULL = 0,     // [3] CTA0: K stage landed (TMA tx)
-    B_KEMPTY = 3,    // [3] CTA0: K stage consumed by the QK MMA
-    B_SFULL = 6,     // [2] CTA0: S buffer ready
-    B_SEMPTY = 8,    // [2] CTA0: S buffer read by the softmax warps (128)
-    B_PEMPTY = 10,   // [4] CTA0: P buffer consumed by CTA1's PV MMA (multicast commit)
-    B_QFULL = 14,    // CTA0: Q tile landed in shared memory (TMA tx)
-    B_QREADY = 15,   // CTA0: Q moved to TMEM, its shared memory free again (128)
-    B_VFULL = 16,    // [2] CTA1: V stage landed
-    B_VEMPTY = 18,   // [2] CTA1: V stage consumed
-    B_PFULL = 20,    // [4] CTA1: P + rescale data written by CTA0 (one cluster-scope arrive)
-    B_REQ = 24,      // CTA1: request to the helper warps (MMA thread arrives)
-    B_DONE = 25,     // CTA1: request served (128)
-    B_OSTEP = 26,    // CTA1: PV MMAs issued so far completed
-    B_STATS = 27,    // CTA1: final row statistics written by CTA0 (one cluster-scope arrive)
-    B_COUNT = 28
+    B_SLOTFULL = 0,     // [9] CTA0: ring slot landed (TMA tx)
+    B_SLOTEMPTY = 9,    // [9] CTA0: ring slot consumed by the QK MMAs
+    B_SFULL = 18,       // [2] CTA0: S buffer ready
+    B_SEMPTY = 20,      // [2] CTA0: S buffer read by the softmax warps (256)
+    B_QFULL = 22,       // CTA0: Q landed in shared memory (TMA tx)
+    B_QREADY = 23,      // CTA0: Q latent dims moved to TMEM, ring slots 0-7 free (256)
+    B_STAGEFREE = 24,   // [3] CTA0: staging buffer copied out (arrive from CTA1)
+    B_PEMPTY = 27,      // [4] CTA0: CTA1's P buffer consumed by its PV MMA (multicast commit)
+    B_VFULL = 31,       // [2] CTA1: V stage landed
+    B_VEMPTY = 33,      // [2] CTA1: V stage consumed
+    B_PFULL = 35,       // [4] CTA1: P message landed (bulk copy tx)
+    B_REQ = 39,         // CTA1: request to the helper warps
+    B_DONE = 40,        // CTA1: request served (128)
+    B_OSTEP = 41,       // CTA1: PV MMAs issued so far completed
+    B_STATS = 42,       // CTA1: final row statistics written by CTA0 (one cluster-scope arrive)
+    B_COUNT = 43
 };
-constexpr int OFF_TMEM = 256;
-constexpr int OFF_ABORT = 260;
-constexpr int OFF_REQ = 264;       // u32 request word (CTA1)
-constexpr int OFF_FLAGS = 288;     // u32 [4]: per P buffer "some row moved its max" (CTA1)
-constexpr int OFF_ALPHA = 512;     // f32 [4][128]: per P buffer, per head rescale factor (CTA1)
-constexpr int OFF_STAT_M = 2560;   // f32 [128]: final running max, log2 units (CTA1)
-constexpr int OFF_STAT_L = 3072;   // f32 [128]: row sum of the bf16-rounded P (normalises O)
-constexpr int OFF_STAT_LT = 3584;  // f32 [128]: row sum of the unrounded P (gives the LSE)
-constexpr int OFF_DATA = kCtrlBytes;
-constexpr int OFF_P = OFF_DATA + kVStages * kVStageBytes;  // CTA1
+constexpr int OFF_TMEM = 512;
+constexpr int OFF_ABORT = 516;
+constexpr int OFF_REQ = 520;
+constexpr int OFF_MX = 1024;       // CTA0: f32 [2][128] exchange between the two page halves
+constexpr int OFF_STAT_M = 2048;   // CTA1: f32 [128] final running max (log2 units)
+constexpr int OFF_STAT_L = 2560;   // CTA1: f32 [128] row sum of the bf16-rounded P (normalises O)
+constexpr int OFF_STAT_LT = 3072;  // CTA1: f32 [128] row sum of the unrounded P (gives the LSE)
 
 // request word: bit 0 rescale, bit 1 zero tail, bit 2 end (epilogue), bit 3 "O holds data",
 // bits 4-7 P buffer, bits 8-11 V stage, bits 12-19 valid rows, bit 20 OSTEP parity (end)
 constexpr uint32_t REQ_FIX = 1u, REQ_TAIL = 2u, REQ_END = 4u, REQ_HAS_O = 8u;
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kQCol = 0;    // CTA0: Q, 288 columns (576 bf16 per lane)
-constexpr uint32_t kSCol = 384;  // CTA0: S buffer b at 384 + 64 b
-constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
+constexpr uint32_t kSCol = 256;  // CTA0: Q latent in columns [0, 256); S buffer b at 256 + 128 b
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr uint32_t kSoftmaxBar = 1;        // named barrier of the 128 softmax threads
+constexpr uint32_t kBarMax = 1, kBarOr = 2, kBarHalf0 = 3;  // named barriers of the softmax warps
 
 struct RowGeom {
     int r, s, b, t, j0, j1, npages, page0;
@@ -132,10 +145,10 @@ __device__ __forceinline__ RowGeom row_geometry(const DecodeArgs& p, int unit, b
 
 // Physical first row of page `pg` of request b, or one past the cache (the TMA then fills
 // zeros) if the block-table entry is out of range.
-__device__ __forceinline__ int page_row(const DecodeArgs& p, int b, int pg) {
+__device__ __forceinline__ int page_row(const DecodeArgs& p, int b, int pg, bool report) {
     int32_t blk = p.block_table[(size_t)b * p.max_blocks + pg];
     if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-        if (p.dev_status) atomicOr(p.dev_status, MLA_DEV_BAD_BLOCK_ID);
+        if (report && p.dev_status) atomicOr(p.dev_status, MLA_DEV_BAD_BLOCK_ID);
         return (int)(p.num_blocks * kPage);
     }
     return blk * kPage;
@@ -147,11 +160,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-// CTA 0's K ring: Q first occupies stages 0 and 1, so page i goes to stage (i + 2) % 3 and is
-// that stage's `kload`-th page.
-__device__ __forceinline__ void k_slot(int i, int& st, int& kload) {
-    st = (i + 2) % kKStages;
-    kload = (i + 2) / kKStages - (st < 2 ? 1 : 0);
+// Ring position of panel p of group g: Q's latent panels first occupy slots 0-7, so the K
+// stream starts at sequence number 8. `k` counts the K fills of that slot.
+__device__ __forceinline__ void ring_pos(int g, int p, int& slot, int& k) {
+    const int n = 8 + 9 * g + p;
+    slot = n % kSlots;
+    k = n / kSlots - (slot < 8 ? 1 : 0);
+}
+
+__device__ __forceinline__ int valid_rows(const RowGeom& g, int page) {
+    return page < g.npages ? min(kPage, g.j1 - (g.j0 + kPage * page)) : 0;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -170,13 +188,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     volatile int* abort = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
     int32_t* ds = p.dev_status;
     auto bar = [&](int i) -> uint32_t { return sbase + 8u * (uint32_t)i; };
+    const int npages = g.npages;
+    const int ngroups = (npages + 1) / 2;
 
     if (tid == 0) {
         *abort = 0;
         for (int i = 0; i < B_COUNT; ++i) {
-            const bool many = (i >= B_SEMPTY && i < B_SEMPTY + 2) || i == B_QREADY || i == B_DONE;
-            bar_init(bar(i), many ? 128u : 1u);
+            const bool many = i == B_SEMPTY || i == B_SEMPTY + 1 || i == B_QREADY;
+            bar_init(bar(i), i == B_DONE ? 128u : (many ? 256u : 1u));
         }
+        if (rank == 1)  // P buffers armed for their first message before CTA 0 can send one
+            for (int b = 0; b < kPBufs; ++b) bar_arrive_expect_tx(bar(B_PFULL + b), kPMsgBytes);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -186,9 +208,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    cluster_sync();  // both CTAs' barriers exist before any remote arrive
+    cluster_sync();  // both CTAs' barriers exist before any remote arrive or copy
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM);
-    const int npages = g.npages;
 
     if (rank == 0) {
         // ============================== scores CTA ==============================
@@ -196,128 +217,168 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0 && npages > 0) {
                 tma_prefetch_desc(&q_map);
                 tma_prefetch_desc(&kv_map);
-                bar_arrive_expect_tx(bar(B_QFULL), 9 * kQPanelBytes);
-#pragma unroll
-                for (int pn = 0; pn < 9; ++pn)
-                    tma_load_2d(sbase + OFF_DATA + pn * kQPanelBytes, &q_map, bar(B_QFULL), pn * 64, g.r * p.H);
-                int issued = 0;
-                for (int i = 0; i < npages; ++i) {
-                    int st, kload;
-                    k_slot(i, st, kload);
-                    if (kload == 0 && st < 2) {
-                        if (!wait_bar(bar(B_QREADY), 0, abort, ds)) break;  // Q region released
-                    } else if (kload > 0 && !wait_bar(bar(B_KEMPTY + st), (kload - 1) & 1, abort, ds)) {
-                        break;
+                for (int pg = 0; pg < min(npages, 2 * kPrefetchGroups); ++pg) {
+                    const int y = page_row(p, g.b, g.page0 + pg, false);
+                    for (int pn = 0; pn < 9; ++pn) tma_prefetch_l2_2d(&kv_map, pn * 64, y);
+                }
+                bar_arrive_expect_tx(bar(B_QFULL), 9 * kSlotBytes);
+                for (int pn = 0; pn < 8; ++pn)
+                    tma_load_2d(sbase + OFF_RING + pn * kSlotBytes, &q_map, bar(B_QFULL), pn * 64, g.r * p.H);
+                tma_load_2d(sbase + OFF_QROPE, &q_map, bar(B_QFULL), 8 * 64, g.r * p.H);
+                int issued_n = 0;  // panels issued
+                bool ok = true;
+                for (int gi = 0; gi < ngroups && ok; ++gi) {
+                    const int pa = 2 * gi, pbp = 2 * gi + 1;
+                    const bool two = pbp < npages;
+                    const int ya = page_row(p, g.b, g.page0 + pa, true);
+                    const int yb = two ? page_row(p, g.b, g.page0 + pbp, true) : 0;
+                    const int pf = 2 * (gi + kPrefetchGroups);  // prefetch one group further
+                    for (int pg = pf; pg < min(npages, pf + 2); ++pg) {
+                        const int y = page_row(p, g.b, g.page0 + pg, false);
+                        for (int pn = 0; pn < 9; ++pn) tma_prefetch_l2_2d(&kv_map, pn * 64, y);
                     }
-                    const uint32_t full = bar(B_KFULL + st);
-                    bar_arrive_expect_tx(full, kKStageBytes);
-                    const int y = page_row(p, g.b, g.page0 + i);
-                    const uint32_t dst = sbase + OFF_DATA + st * kKStageBytes;
-#pragma unroll
-                    for (int pn = 0; pn < 9; ++pn) tma_load_2d(dst + pn * kPanelBytes, &kv_map, full, pn * 64, y);
-                    issued = i + 1;
+                    for (int pn = 0; pn < 9; ++pn) {
+                        int slot, k;
+                        ring_pos(gi, pn, slot, k);
+                        if (k > 0)
+                            ok = wait_bar(bar(B_SLOTEMPTY + slot), (k - 1) & 1, abort, ds);
+                        else if (slot < 8)
+                            ok = wait_bar(bar(B_QREADY), 0, abort, ds);  // Q's panel moved out
+                        if (!ok) break;
+                        const uint32_t full = bar(B_SLOTFULL + slot);
+                        const uint32_t dst = sbase + OFF_RING + slot * kSlotBytes;
+                        bar_arrive_expect_tx(full, (two ? 2 : 1) * kPageBox);
+                        tma_load_2d(dst, &kv_map, full, pn * 64, ya);
+                        if (two) tma_load_2d(dst + kPageBox, &kv_map, full, pn * 64, yb);
+                        ++issued_n;
+                    }
                 }
                 if (*abort) {  // let the copies in flight land before the CTA can exit
                     volatile int dummy = 0;
                     wait_bar(bar(B_QFULL), 0, &dummy, nullptr);
-                    for (int i = (issued > kKStages ? issued - kKStages : 0); i < issued; ++i) {
-                        int st, kload;
-                        k_slot(i, st, kload);
+                    for (int n = (issued_n > kSlots ? issued_n - kSlots : 0); n < issued_n; ++n) {
+                        int slot, k;
+                        ring_pos(n / 9, n % 9, slot, k);
                         dummy = 0;
-                        wait_bar(bar(B_KFULL + st), kload & 1, &dummy, nullptr);
+                        wait_bar(bar(B_SLOTFULL + slot), k & 1, &dummy, nullptr);
                     }
                 }
             }
         } else if (warp == 1) {
             if (lane == 0 && npages > 0) {
-                int done = 0;
-                if (wait_bar(bar(B_QREADY), 0, abort, ds)) {
-                    tc_fence_after();
-                    for (int i = 0; i < npages; ++i) {
-                        int st, kload;
-                        k_slot(i, st, kload);
-                        const int sb = i & 1, us = i >> 1;
-                        if (!wait_bar(bar(B_KFULL + st), kload & 1, abort, ds)) break;
-                        if (us > 0 && !wait_bar(bar(B_SEMPTY + sb), (us - 1) & 1, abort, ds)) break;
+                int done_n = 0;
+                bool ok = wait_bar(bar(B_QREADY), 0, abort, ds);
+                for (int gi = 0; gi < ngroups && ok; ++gi) {
+                    const int sb = gi & 1, us = gi >> 1;
+                    if (us > 0 && !(ok = wait_bar(bar(B_SEMPTY + sb), (us - 1) & 1, abort, ds))) break;
+                    const uint32_t d = tmem + kSCol + 128u * sb;
+                    for (int pn = 0; pn < 9; ++pn) {
+                        int slot, k;
+                        ring_pos(gi, pn, slot, k);
+                        if (!(ok = wait_bar(bar(B_SLOTFULL + slot), k & 1, abort, ds))) break;
                         tc_fence_after();
-                        const uint32_t d = tmem + kSCol + 64u * sb;
-                        const uint32_t kb = sbase + OFF_DATA + st * kKStageBytes;
-#pragma unroll 4
-                        for (int kk = 0; kk < kD / 16; ++kk) {
-                            const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-                            mma_ts(d, tmem + kQCol + 8u * kk, bd, kIdescQK, kk > 0 ? 1u : 0u);
+                        const uint32_t kb = sbase + OFF_RING + slot * kSlotBytes;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint64_t bd = smem_desc_sw128(kb + 32 * j, 16, 1024);
+                            if (pn < 8) {
+                                mma_ts(d, tmem + 8u * (4 * pn + j), bd, kIdescQK, (pn | j) ? 1u : 0u);
+                            } else {
+                                const uint64_t ad = smem_desc_sw128(sbase + OFF_QROPE + 32 * j, 16, 1024);
+                                mma_ss(d, ad, bd, kIdescQK, 1u);
+                            }
                         }
-                        mma_commit(bar(B_SFULL + sb));
-                        mma_commit(bar(B_KEMPTY + st));
-                        done = i + 1;
+                        mma_commit(bar(B_SLOTEMPTY + slot));
+                        ++done_n;
                     }
+                    if (ok) mma_commit(bar(B_SFULL + sb));
                 }
                 volatile int dummy = 0;  // drain: the last commits have landed before teardown
-                for (int i = (done > kKStages ? done - kKStages : 0); i < done; ++i) {
-                    int st, kload;
-                    k_slot(i, st, kload);
+                for (int n = (done_n > kSlots ? done_n - kSlots : 0); n < done_n; ++n) {
+                    int slot, k;
+                    ring_pos(n / 9, n % 9, slot, k);
                     dummy = 0;
-                    wait_bar(bar(B_KEMPTY + st), kload & 1, &dummy, nullptr);
+                    wait_bar(bar(B_SLOTEMPTY + slot), k & 1, &dummy, nullptr);
                 }
             }
         } else {
-            // ------------------------------ softmax warps ------------------------------
-            const int row = 32 * (warp & 3) + lane;  // head
+            // ------------------------- softmax warps (256 threads) -------------------------
+            const int half = (warp - 2) >> 2;              // page of the group this warp owns
+            const int row = 32 * (warp & 3) + lane;        // head
             const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
             const bool live = row < p.H;
+            float* mx = reinterpret_cast<float*>(smem + OFF_MX);
             if (npages > 0) {
-                // Q row from the TMA tile (swizzled 16-byte chunks) into TMEM; zeros past H
+                // Q latent dims: this half moves panels 4 half .. 4 half + 3 into TMEM
                 const bool okq = warp_wait(bar(B_QFULL), 0, abort, ds);
 #pragma unroll 1
-                for (int pn = 0; pn < 9; ++pn) {
+                for (int pn = 4 * half; pn < 4 * half + 4; ++pn) {
                     uint32_t v[32];
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         uint4 x = make_uint4(0, 0, 0, 0);
                         if (live && okq)
-                            x = *reinterpret_cast<const uint4*>(smem + OFF_DATA + pn * kQPanelBytes + row * 128 +
+                            x = *reinterpret_cast<const uint4*>(smem + OFF_RING + pn * kSlotBytes + row * 128 +
                                                                 ((c ^ (row & 7)) << 4));
                         v[4 * c] = x.x;
                         v[4 * c + 1] = x.y;
                         v[4 * c + 2] = x.z;
                         v[4 * c + 3] = x.w;
                     }
-                    tmem_st32(tmem + lane_base + kQCol + 32u * pn, v);
+                    tmem_st32(tmem + lane_base + 32u * pn, v);
+                }
+                if (!live && half == 0) {  // heads past H: zero rope rows too (S rows stay finite)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(smem + OFF_QROPE + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_cta();
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 bar_arrive(bar(B_QREADY));
             }
             const float sl2 = p.scale * 1.4426950408889634f;  // exp2 domain
-            // l_run sums P exactly as the PV MMA sees it (bf16) so that o = P V / l_run stays
-            // consistent when one token dominates; lt_run sums the unrounded P for the LSE.
+            // l sums P as the PV MMA sees it (bf16) so that o = P V / l stays consistent when one
+            // token dominates; lt sums the unrounded P for the LSE. Each half keeps its own sums
+            // (same running max); they are added at the end.
             float m_run = -CUDART_INF_F, l_run = 0.f, lt_run = 0.f;
-            const uint32_t p_remote = map_to_rank(sbase + OFF_P, 1);
-            const uint32_t alpha_remote = map_to_rank(sbase + OFF_ALPHA, 1);
-            const uint32_t flags_remote = map_to_rank(sbase + OFF_FLAGS, 1);
-            for (int i = 0; i < npages; ++i) {
-                const int sb = i & 1, us = i >> 1, pb = i % kPBufs, up = i / kPBufs;
-                if (!warp_wait(bar(B_SFULL + sb), us & 1, abort, ds)) break;
-                tc_fence_after();
+            const uint32_t pbuf_remote = map_to_rank(sbase + OFF_PB, 1);
+            const uint32_t pfull_remote = map_to_rank(bar(B_PFULL), 1);
+            for (int gi = 0; gi < ngroups; ++gi) {
+                const int sb = gi & 1, us = gi >> 1;
+                const int page = 2 * gi + half;
+                const int valid = valid_rows(g, page);
+                // No early exit from this loop: all 256 threads must pass the same named barriers
+                // (which cannot time out); after an abort the waits return at once and the work
+                // is skipped.
+                const bool okS = warp_wait(bar(B_SFULL + sb), us & 1, abort, ds);
                 uint32_t s0[32], s1[32];
-                tmem_ld32(tmem + lane_base + kSCol + 64u * sb, s0);
-                tmem_ld32(tmem + lane_base + kSCol + 64u * sb + 32u, s1);
-                tmem_wait_ld();
-                tc_fence_before();
-                bar_arrive(bar(B_SEMPTY + sb));
-                const int valid = min(kPage, g.j1 - (g.j0 + kPage * i));
-                float mt = -CUDART_INF_F;
+                if (okS) {
+                    tc_fence_after();
+                    const uint32_t scol = tmem + lane_base + kSCol + 128u * sb + 64u * half;
+                    tmem_ld32(scol, s0);
+                    tmem_ld32(scol + 32u, s1);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    bar_arrive(bar(B_SEMPTY + sb));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) s0[c] = s1[c] = __float_as_uint(-CUDART_INF_F);
+                }
+                float lm = -CUDART_INF_F;
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     if (c >= valid) s0[c] = __float_as_uint(-CUDART_INF_F);
                     if (c + 32 >= valid) s1[c] = __float_as_uint(-CUDART_INF_F);
-                    mt = fmaxf(mt, fmaxf(__uint_as_float(s0[c]), __uint_as_float(s1[c])));
+                    lm = fmaxf(lm, fmaxf(__uint_as_float(s0[c]), __uint_as_float(s1[c])));
                 }
-                mt *= sl2;  // scale > 0: the max commutes with the scaling
+                mx[half * 128 + row] = lm;
+                named_bar(kBarMax, 256);
+                const float mt = fmaxf(lm, mx[(1 - half) * 128 + row]) * sl2;  // scale > 0
                 const bool resc = mt > m_run + kRescaleThreshold;
                 float alpha = 1.f;
                 if (resc) {
-                    alpha = fast_exp2(m_run - mt);  // 0 on the first page (m_run = -inf)
+                    alpha = fast_exp2(m_run - mt);  // 0 on the first group (m_run = -inf)
                     m_run = mt;
                 }
                 uint32_t pk[32];
@@ -335,29 +396,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 l_run = l_run * alpha + sum;
                 lt_run = lt_run * alpha + sum_t;
-                if (up > 0 && !warp_wait<true>(bar(B_PEMPTY + pb), (up - 1) & 1, abort, ds)) break;
-                const uint32_t pdst = p_remote + pb * kPBytes + row * 128;
+                const bool exists = page < npages;
+                const int stg = page % kStageBufs, ust = page / kStageBufs;
+                bool ok = okS;
+                if (ok && exists && ust > 0) ok = warp_wait<true>(bar(B_STAGEFREE + stg), (ust - 1) & 1, abort, ds);
+                uint8_t* sbuf = smem + OFF_STAGE + stg * kPBufStride;
+                if (exists && ok) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_cluster_v4(pdst + ((uint32_t)(c ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                                  pk[4 * c + 3]);
-                st_cluster_u32(alpha_remote + 4u * (pb * 128 + row), __float_as_uint(alpha));
-                fence_proxy_async_cluster();
-                const bool any = named_bar_or(kSoftmaxBar, 128, resc && i > 0);
-                if (tid == 64) {  // one cluster-scope release covers the whole group's writes
-                    st_cluster_u32(flags_remote + 4u * pb, any ? 1u : 0u);
-                    bar_arrive_remote(bar(B_PFULL + pb), 1);
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(sbuf + row * 128 + ((c ^ (row & 7)) << 4)) =
+                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    reinterpret_cast<float*>(sbuf + kPBytes)[row] = half == 0 ? alpha : 1.f;
+                    fence_proxy_async_cta();
+                }
+                // every row's alpha is shipped with the group's first page; the flag tells CTA 1
+                // whether any of them differs from 1
+                const bool any = named_bar_or(kBarOr, 256, resc && gi > 0);
+                if (tid == 64 && !*abort) {
+                    for (int q = 0; q < 2; ++q) {
+                        const int pg = 2 * gi + q;
+                        if (pg >= npages) break;
+                        uint8_t* b = smem + OFF_STAGE + (pg % kStageBufs) * kPBufStride;
+                        *reinterpret_cast<uint32_t*>(b + kPBytes + 512) = (q == 0 && any) ? 1u : 0u;
+                        fence_proxy_async_cta();
+                        const int pbi = pg % kPBufs, upb = pg / kPBufs;
+                        if (upb > 0 && !wait_bar<true>(bar(B_PEMPTY + pbi), (upb - 1) & 1, abort, ds)) break;
+                        bulk_copy_to_peer(pbuf_remote + pbi * kPBufStride, smem_addr(b), kPMsgBytes,
+                                          pfull_remote + 8u * pbi);
+                    }
                 }
             }
-            st_cluster_u32(map_to_rank(sbase + OFF_STAT_M, 1) + 4u * row, __float_as_uint(m_run));
-            st_cluster_u32(map_to_rank(sbase + OFF_STAT_L, 1) + 4u * row, __float_as_uint(l_run));
-            st_cluster_u32(map_to_rank(sbase + OFF_STAT_LT, 1) + 4u * row, __float_as_uint(lt_run));
-            named_bar(kSoftmaxBar, 128);
-            if (tid == 64) bar_arrive_remote(bar(B_STATS), 1);
-            // no multicast commit may still be on its way to this CTA when it exits
-            for (int i = (npages > kPBufs ? npages - kPBufs : 0); i < npages; ++i) {
-                volatile int dummy = 0;
-                wait_bar<true>(bar(B_PEMPTY + i % kPBufs), (i / kPBufs) & 1, *abort ? &dummy : abort, ds);
+            // combine the two halves' sums, ship the final statistics
+            named_bar(kBarMax, 256);
+            if (half == 1) {
+                mx[row] = l_run;
+                mx[128 + row] = lt_run;
+            }
+            named_bar(kBarMax, 256);
+            if (half == 0) {
+                l_run += mx[row];
+                lt_run += mx[128 + row];
+                st_cluster_u32(map_to_rank(sbase + OFF_STAT_M, 1) + 4u * row, __float_as_uint(m_run));
+                st_cluster_u32(map_to_rank(sbase + OFF_STAT_L, 1) + 4u * row, __float_as_uint(l_run));
+                st_cluster_u32(map_to_rank(sbase + OFF_STAT_LT, 1) + 4u * row, __float_as_uint(lt_run));
+                named_bar(kBarHalf0, 128);
+                if (tid == 64) {
+                    bar_arrive_remote(bar(B_STATS), 1);
+                    // nothing may still be on its way to this CTA when it exits
+                    for (int pg = (npages > kPBufs ? npages - kPBufs : 0); pg < npages; ++pg) {
+                        volatile int dummy = 0;
+                        wait_bar<true>(bar(B_PEMPTY + pg % kPBufs), (pg / kPBufs) & 1, *abort ? &dummy : abort, ds);
+                    }
+                    for (int pg = (npages > kStageBufs ? npages - kStageBufs : 0); pg < npages; ++pg) {
+                        volatile int dummy = 0;
+                        wait_bar<true>(bar(B_STAGEFREE + pg % kStageBufs), (pg / kStageBufs) & 1,
+                                       *abort ? &dummy : abort, ds);
+                    }
+                }
             }
         }
     } else {
@@ -371,10 +466,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (kv > 0 && !wait_bar(bar(B_VEMPTY + st), (kv - 1) & 1, abort, ds)) break;
                     const uint32_t full = bar(B_VFULL + st);
                     bar_arrive_expect_tx(full, kVStageBytes);
-                    const int y = page_row(p, g.b, g.page0 + i);
-                    const uint32_t dst = sbase + OFF_DATA + st * kVStageBytes;
+                    const int y = page_row(p, g.b, g.page0 + i, false);
+                    const uint32_t dst = sbase + OFF_V + st * kVStageBytes;
 #pragma unroll
-                    for (int pn = 0; pn < 8; ++pn) tma_load_2d(dst + pn * kPanelBytes, &kv_map, full, pn * 64, y);
+                    for (int pn = 0; pn < 8; ++pn) tma_load_2d(dst + pn * kPageBox, &kv_map, full, pn * 64, y);
                     issued = i + 1;
                 }
                 if (*abort) {
@@ -386,16 +481,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
         } else if (warp == 1) {
             if (lane == 0) {
-                uint32_t* req_word = reinterpret_cast<uint32_t*>(smem + OFF_REQ);
+                volatile uint32_t* req_word = reinterpret_cast<volatile uint32_t*>(smem + OFF_REQ);
                 int n_req = 0, n_ostep = 0, done = 0;
                 bool ok = true;
                 for (int i = 0; i < npages && ok; ++i) {
                     const int st = i % kVStages, kv = i / kVStages, pb = i % kPBufs, up = i / kPBufs;
                     ok = wait_bar(bar(B_VFULL + st), kv & 1, abort, ds) &&
-                         wait_bar<true>(bar(B_PFULL + pb), up & 1, abort, ds);
+                         wait_bar(bar(B_PFULL + pb), up & 1, abort, ds);
                     if (!ok) break;
-                    const bool fix = i > 0 && reinterpret_cast<volatile uint32_t*>(smem + OFF_FLAGS)[pb] != 0;
-                    const int valid = min(kPage, g.j1 - (g.j0 + kPage * i));
+                    // the staging buffer in CTA 0 has been copied out: let it be reused
+                    bar_arrive_remote(bar(B_STAGEFREE + i % kStageBufs), 0);
+                    const uint8_t* pmsg = smem + OFF_PB + pb * kPBufStride;
+                    const bool fix = i > 0 && *reinterpret_cast<const volatile uint32_t*>(pmsg + kPBytes + 512) != 0;
+                    const int valid = valid_rows(g, i);
                     if (fix || valid < kPage) {
                         if (fix) {  // the rescale must see every earlier PV product in O
                             mma_commit(bar(B_OSTEP));
@@ -403,28 +501,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             ++n_ostep;
                             if (!ok) break;
                         }
-                        *reinterpret_cast<volatile uint32_t*>(req_word) =
-                            (fix ? REQ_FIX : 0u) | (valid < kPage ? REQ_TAIL : 0u) | ((uint32_t)pb << 4) |
-                            ((uint32_t)st << 8) | ((uint32_t)valid << 12);
+                        *req_word = (fix ? REQ_FIX : 0u) | (valid < kPage ? REQ_TAIL : 0u) | ((uint32_t)pb << 4) |
+                                    ((uint32_t)st << 8) | ((uint32_t)valid << 12);
                         bar_arrive(bar(B_REQ));
                         ok = wait_bar(bar(B_DONE), n_req & 1, abort, ds);
                         ++n_req;
                         if (!ok) break;
                     }
                     tc_fence_after();
-                    const uint32_t vb = sbase + OFF_DATA + st * kVStageBytes;
-                    const uint32_t pbuf = sbase + OFF_P + pb * kPBytes;
+                    const uint32_t vb = sbase + OFF_V + st * kVStageBytes;
+                    const uint32_t pbuf = sbase + OFF_PB + pb * kPBufStride;
 #pragma unroll
                     for (int kk = 0; kk < kPage / 16; ++kk) {
                         const uint64_t ad = smem_desc_sw128(pbuf + kk * 32, 16, 1024);
 #pragma unroll
                         for (int nh = 0; nh < 2; ++nh) {
-                            const uint64_t bd = smem_desc_sw128(vb + nh * 4 * kPanelBytes + kk * 2048, kPanelBytes, 1024);
+                            const uint64_t bd = smem_desc_sw128(vb + nh * 4 * kPageBox + kk * 2048, kPageBox, 1024);
                             mma_ss(tmem + 256u * nh, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
                     mma_commit(bar(B_VEMPTY + st));
                     mma_commit_multicast(bar(B_PEMPTY + pb), (uint16_t)0x1);
+                    bar_arrive_expect_tx(bar(B_PFULL + pb), kPMsgBytes);  // armed for its next message
                     done = i + 1;
                 }
                 uint32_t end = REQ_END;
@@ -433,7 +531,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     end |= ((uint32_t)(n_ostep & 1) << 20) | (ok && done == npages ? REQ_HAS_O : 0u);
                     ++n_ostep;
                 }
-                *reinterpret_cast<volatile uint32_t*>(req_word) = end;
+                *req_word = end;
                 bar_arrive(bar(B_REQ));
                 volatile int dummy = 0;  // drain the V-ring commits before teardown
                 for (int i = (done > kVStages ? done - kVStages : 0); i < done; ++i) {
@@ -441,7 +539,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     wait_bar(bar(B_VEMPTY + i % kVStages), (i / kVStages) & 1, &dummy, nullptr);
                 }
             }
-        } else {
+        } else if (warp < 6) {
             // ------------------ helper warps: rescale, tail zeroing, epilogue ------------------
             const int row = 32 * (warp & 3) + lane;
             const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -457,7 +555,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int pb = (req >> 4) & 15, st = (req >> 8) & 15, valid = (req >> 12) & 255;
                 if (req & REQ_FIX) {
                     tc_fence_after();
-                    const float a = reinterpret_cast<volatile float*>(smem + OFF_ALPHA)[pb * 128 + row];
+                    const float a = reinterpret_cast<volatile float*>(smem + OFF_PB + pb * kPBufStride + kPBytes)[row];
 #pragma unroll 1
                     for (int c = 0; c < kL / 32; ++c) {
                         uint32_t v[32];
@@ -470,11 +568,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tmem_wait_st();
                 }
                 if (req & REQ_TAIL) {  // zero V rows [valid, 64) of all 8 panels of the stage
-                    const uint32_t vb = OFF_DATA + st * kVStageBytes;
+                    const uint32_t vb = OFF_V + st * kVStageBytes;
                     const int chunks = (kPage - valid) * 8 * 8;
                     for (int q = ctid; q < chunks; q += 128) {
                         const int rr = valid + q / 64, pn = (q / 8) % 8, cc = q % 8;
-                        *reinterpret_cast<uint4*>(smem + vb + pn * kPanelBytes + rr * 128 + cc * 16) =
+                        *reinterpret_cast<uint4*>(smem + vb + pn * kPageBox + rr * 128 + cc * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_cta();

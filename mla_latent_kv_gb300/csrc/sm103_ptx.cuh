@@ -155,6 +155,24 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
         : "memory");
 }
 
+// Prefetch one box of a tensor into L2 (no shared memory, no completion tracking).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to another CTA's shared
+// memory of the cluster; completion is counted (complete_tx) on the barrier `remote_bar`, which
+// lives in the destination CTA. Both addresses are shared::cluster addresses (see map_to_rank).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,
+                                                  uint32_t remote_bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     remote_dst),
+                 "r"(local_src), "r"(bytes), "r"(remote_bar)
+                 : "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (tensor
 // core / TMA) of the CTA that owns the memory.
 __device__ __forceinline__ void fence_proxy_async_cluster() {
