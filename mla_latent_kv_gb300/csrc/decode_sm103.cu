@@ -5,31 +5,32 @@
 // row's visible tokens [j0, j1) (one split of it), every head reading the same 576-element
 // cached row:  S = scale * Q K^T,  P = softmax(S),  O = P V  with V = the first 512 dims.
 //
-// One thread-block cluster of two CTAs per (query row, split) unit; pages are taken two at a
-// time ("groups" of 128 tokens) so that every tensor-core instruction has N >= 128, the shape
-// at which tcgen05.mma runs at its full rate.
+// One thread-block cluster of two CTAs per (query row, split) unit. Pages are taken four at a
+// time ("groups" of 256 tokens) so that every tensor-core instruction has N = 256: with N = 256
+// the tensor core holds enough queued work to hide the ~130-cycle gap that each blocking
+// synchronisation of the issuing thread leaves, so the pipe stays busy between ring slots.
 //
 //   CTA 0 ("scores")  Q: the 512 latent dims (128 heads x 512 bf16) are loaded once by TMA and
 //                     kept in tensor memory; the 64 rope dims stay in shared memory.
-//                     K: the group's two pages stream through a ring of nine 16 KB slots, one
-//                     slot per 64-dim panel holding both pages' rows (128 rows, 128-byte
-//                     swizzle), refilled panel by panel as the MMAs release them, with the pages
-//                     further ahead prefetched into L2.
-//                     S = Q K^T per group: 36 tcgen05.mma of M=128 heads x N=128 tokens x K=16
-//                     (32 with A from TMEM, 4 with A = rope dims from shared memory) into one of
-//                     two 128-column TMEM buffers.
-//                     Softmax: eight warps, two per TMEM lane quarter, each owning one page of
+//                     K: a ring of four 32 KB slots, one slot = one 64-dim panel of a group's
+//                     four pages (256 rows, 128-byte swizzle), refilled panel by panel as the
+//                     MMAs release them.
+//                     S = Q K^T per group: 36 tcgen05.mma of M=128 heads x N=256 tokens x K=16
+//                     (32 with A from TMEM, 4 with A = rope dims from shared memory) into a
+//                     256-column TMEM buffer.
+//                     Softmax: eight warps, two per TMEM lane quarter, each owning two pages of
 //                     the group for 32 heads; fp32 online softmax with a lazily moved running
 //                     max (rescale only when a row's max grows by more than 2^8). P (bf16, in
 //                     the MMA's swizzled K-major layout) and the per-head rescale factors are
-//                     written to a local staging buffer and sent to CTA 1 with one bulk
+//                     written to local staging buffers and sent to CTA 1 with one bulk
 //                     shared-to-shared copy per page (counted by bytes on CTA 1's barrier).
 //   CTA 1 ("output")  holds the 128 x 512 fp32 output accumulator -- all 512 TMEM columns of its
 //                     SM, the reason the work is split over two SMs -- streams the pages'
 //                     first 512 dims (mostly L2 hits), and accumulates O += P V per page with
 //                     tcgen05.mma (M=128, N=2x256, K=64; V read as an MN-major operand straight
-//                     from the TMA tile). Four helper warps act on request: rescale O, zero the
-//                     V rows past the end of the last page, and the epilogue.
+//                     from the TMA tile). Its MMA thread waits on a single barrier per page; four
+//                     helper warps do everything else: wait for P and V, hand the staging buffer
+//                     back, rescale O, zero the V rows past the last token, and the epilogue.
 // Per page the pair issues exactly the algorithm's 2*128*64*(576+512) flops.
 //
 // Rows past the split's last visible token are masked by index (S = -inf) and, in the last
@@ -55,23 +56,23 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (CTA 0) / 2-5 helpers (CTA 1)
-constexpr int kSlots = 9;            // CTA 0 K ring: one slot = one 64-dim panel of a 2-page group
-constexpr int kSlotBytes = 128 * 128;
-constexpr int kPageBox = 64 * 128;   // one page's rows of one panel
-constexpr int kPrefetchGroups = 3;   // groups prefetched into L2 ahead of the ring
-constexpr int kStageBufs = 3;        // CTA 0 P staging buffers (one page each)
-constexpr int kPBufs = 4;            // CTA 1 P buffers (one page each)
+constexpr int kPPG = 4;              // pages per group
+constexpr int kSlots = 4;            // CTA 0 K ring slots
+constexpr int kPageBox = 64 * 128;   // one page's rows of one 64-dim panel (8 KB)
+constexpr int kSlotBytes = kPPG * kPageBox;  // 32 KB
+constexpr int kQPanelBytes = 128 * 128;      // 128 heads x 64 dims of Q (16 KB)
+constexpr int kPBufs = 4;            // P buffers: CTA 0 staging and CTA 1 receive (one page each)
 constexpr int kVStages = 2;          // CTA 1 V ring (one page each)
-constexpr int kVStageBytes = 8 * kPageBox;  // 65,536
-constexpr int kPBytes = 128 * 128;          // P page: 128 heads x 64 tokens bf16
+constexpr int kVStageBytes = 8 * kPageBox;      // 65,536
+constexpr int kPBytes = 128 * 128;              // P page: 128 heads x 64 tokens bf16
 constexpr int kPMsgBytes = kPBytes + 512 + 16;  // P + alpha[128] + flag word: one bulk copy
 constexpr int kPBufStride = 17 * 1024;
 constexpr int kCtrlBytes = 4096;
 // CTA 0 layout
-constexpr int OFF_QROPE = kCtrlBytes;                      // 16 KB: Q rope panel
-constexpr int OFF_RING = OFF_QROPE + kSlotBytes;           // 9 x 16 KB
-constexpr int OFF_STAGE = OFF_RING + kSlots * kSlotBytes;  // 3 x 17 KB
-constexpr int kSmem0 = OFF_STAGE + kStageBufs * kPBufStride;
+constexpr int OFF_QROPE = kCtrlBytes;                      // 16 KB
+constexpr int OFF_RING = OFF_QROPE + kQPanelBytes;         // 4 x 32 KB
+constexpr int OFF_STAGE = OFF_RING + kSlots * kSlotBytes;  // 4 x 17 KB
+constexpr int kSmem0 = OFF_STAGE + kPBufs * kPBufStride;
 // CTA 1 layout
 constexpr int OFF_V = kCtrlBytes;
 constexpr int OFF_PB = OFF_V + kVStages * kVStageBytes;
@@ -79,42 +80,37 @@ constexpr int kSmem1 = OFF_PB + kPBufs * kPBufStride;
 constexpr int kSmemBytes = kSmem0 > kSmem1 ? kSmem0 : kSmem1;
 static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
 static_assert(kPMsgBytes % 16 == 0 && kPMsgBytes <= kPBufStride, "P message");
+static_assert(8 * kQPanelBytes == kSlots * kSlotBytes, "Q's latent panels fill the K ring exactly");
 
-// Barrier slots (8 bytes each) at the start of the control block; one layout for both CTAs so
-// that a multicast commit from CTA 1 lands on CTA 0's B_PEMPTY slots.
+// Barrier slots (8 bytes each); one layout for both CTAs so that a multicast commit from CTA 1
+// lands on CTA 0's B_PEMPTY slots.
 enum : int {
-    B_SLOTFULL = 0,     // [9] CTA0: ring slot landed (TMA tx)
-    B_SLOTEMPTY = 9,    // [9] CTA0: ring slot consumed by the QK MMAs
-    B_SFULL = 18,       // [2] CTA0: S buffer ready
-    B_SEMPTY = 20,      // [2] CTA0: S buffer read by the softmax warps (256)
-    B_QFULL = 22,       // CTA0: Q landed in shared memory (TMA tx)
-    B_QREADY = 23,      // CTA0: Q latent dims moved to TMEM, ring slots 0-7 free (256)
-    B_STAGEFREE = 24,   // [3] CTA0: staging buffer copied out (arrive from CTA1)
-    B_PEMPTY = 27,      // [4] CTA0: CTA1's P buffer consumed by its PV MMA (multicast commit)
-    B_VFULL = 31,       // [2] CTA1: V stage landed
-    B_VEMPTY = 33,      // [2] CTA1: V stage consumed
-    B_PFULL = 35,       // [4] CTA1: P message landed (bulk copy tx)
-    B_REQ = 39,         // CTA1: request to the helper warps
-    B_DONE = 40,        // CTA1: request served (128)
-    B_OSTEP = 41,       // CTA1: PV MMAs issued so far completed
-    B_STATS = 42,       // CTA1: final row statistics written by CTA0 (one cluster-scope arrive)
-    B_COUNT = 43
+    B_SLOTFULL = 0,     // [4] CTA0: ring slot landed (TMA tx)
+    B_SLOTEMPTY = 4,    // [4] CTA0: ring slot consumed by the QK MMAs
+    B_SFULL = 8,        // CTA0: S ready
+    B_SEMPTY = 9,       // CTA0: S read into registers by the softmax warps (256)
+    B_QFULL = 10,       // CTA0: Q landed in shared memory (TMA tx)
+    B_QREADY = 11,      // CTA0: Q latent dims moved to TMEM, ring free for K (256)
+    B_STAGEFREE = 12,   // [4] CTA0: staging buffer copied out (arrive from CTA1)
+    B_PEMPTY = 16,      // [4] CTA0: CTA1's P buffer consumed by its PV MMA (multicast commit)
+    B_VFULL = 20,       // [2] CTA1: V stage landed
+    B_VEMPTY = 22,      // [2] CTA1: V stage consumed
+    B_PFULL = 24,       // [4] CTA1: P message landed (bulk copy tx)
+    B_READY = 28,       // [4] CTA1: page ready for its PV MMA (128 helper threads)
+    B_OSTEP = 32,       // CTA1: PV MMAs of a page completed (one phase per page)
+    B_STATS = 33,       // CTA1: final row statistics written by CTA0 (one cluster-scope arrive)
+    B_COUNT = 34
 };
 constexpr int OFF_TMEM = 512;
 constexpr int OFF_ABORT = 516;
-constexpr int OFF_REQ = 520;
-constexpr int OFF_MX = 1024;       // CTA0: f32 [2][128] exchange between the two page halves
+constexpr int OFF_MX = 1024;       // CTA0: f32 [2][128] exchange between the two warp halves
 constexpr int OFF_STAT_M = 2048;   // CTA1: f32 [128] final running max (log2 units)
 constexpr int OFF_STAT_L = 2560;   // CTA1: f32 [128] row sum of the bf16-rounded P (normalises O)
 constexpr int OFF_STAT_LT = 3072;  // CTA1: f32 [128] row sum of the unrounded P (gives the LSE)
 
-// request word: bit 0 rescale, bit 1 zero tail, bit 2 end (epilogue), bit 3 "O holds data",
-// bits 4-7 P buffer, bits 8-11 V stage, bits 12-19 valid rows, bit 20 OSTEP parity (end)
-constexpr uint32_t REQ_FIX = 1u, REQ_TAIL = 2u, REQ_END = 4u, REQ_HAS_O = 8u;
-
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol = 256;  // CTA0: Q latent in columns [0, 256); S buffer b at 256 + 128 b
-constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
+constexpr uint32_t kSCol = 256;  // CTA0: Q latent in columns [0, 256), S in [256, 512)
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 256, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kBarMax = 1, kBarOr = 2, kBarHalf0 = 3;  // named barriers of the softmax warps
@@ -145,10 +141,10 @@ __device__ __forceinline__ RowGeom row_geometry(const DecodeArgs& p, int unit, b
 
 // Physical first row of page `pg` of request b, or one past the cache (the TMA then fills
 // zeros) if the block-table entry is out of range.
-__device__ __forceinline__ int page_row(const DecodeArgs& p, int b, int pg, bool report) {
+__device__ __forceinline__ int page_row(const DecodeArgs& p, int b, int pg) {
     int32_t blk = p.block_table[(size_t)b * p.max_blocks + pg];
     if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-        if (report && p.dev_status) atomicOr(p.dev_status, MLA_DEV_BAD_BLOCK_ID);
+        if (p.dev_status) atomicOr(p.dev_status, MLA_DEV_BAD_BLOCK_ID);
         return (int)(p.num_blocks * kPage);
     }
     return blk * kPage;
@@ -158,14 +154,6 @@ template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* ds) {
     bool ok = wait_bar<kCluster>(bar, parity, abort, ds);
     return __all_sync(0xffffffffu, ok);
-}
-
-// Ring position of panel p of group g: Q's latent panels first occupy slots 0-7, so the K
-// stream starts at sequence number 8. `k` counts the K fills of that slot.
-__device__ __forceinline__ void ring_pos(int g, int p, int& slot, int& k) {
-    const int n = 8 + 9 * g + p;
-    slot = n % kSlots;
-    k = n / kSlots - (slot < 8 ? 1 : 0);
 }
 
 __device__ __forceinline__ int valid_rows(const RowGeom& g, int page) {
@@ -189,13 +177,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int32_t* ds = p.dev_status;
     auto bar = [&](int i) -> uint32_t { return sbase + 8u * (uint32_t)i; };
     const int npages = g.npages;
-    const int ngroups = (npages + 1) / 2;
+    const int ngroups = (npages + kPPG - 1) / kPPG;
 
     if (tid == 0) {
         *abort = 0;
         for (int i = 0; i < B_COUNT; ++i) {
-            const bool many = i == B_SEMPTY || i == B_SEMPTY + 1 || i == B_QREADY;
-            bar_init(bar(i), i == B_DONE ? 128u : (many ? 256u : 1u));
+            uint32_t cnt = 1;
+            if (i == B_SEMPTY || i == B_QREADY) cnt = 256;
+            if (i >= B_READY && i < B_READY + kPBufs) cnt = 128;
+            bar_init(bar(i), cnt);
         }
         if (rank == 1)  // P buffers armed for their first message before CTA 0 can send one
             for (int b = 0; b < kPBufs; ++b) bar_arrive_expect_tx(bar(B_PFULL + b), kPMsgBytes);
@@ -217,66 +207,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0 && npages > 0) {
                 tma_prefetch_desc(&q_map);
                 tma_prefetch_desc(&kv_map);
-                for (int pg = 0; pg < min(npages, 2 * kPrefetchGroups); ++pg) {
-                    const int y = page_row(p, g.b, g.page0 + pg, false);
-                    for (int pn = 0; pn < 9; ++pn) tma_prefetch_l2_2d(&kv_map, pn * 64, y);
-                }
-                bar_arrive_expect_tx(bar(B_QFULL), 9 * kSlotBytes);
+                bar_arrive_expect_tx(bar(B_QFULL), 9 * kQPanelBytes);
                 for (int pn = 0; pn < 8; ++pn)
-                    tma_load_2d(sbase + OFF_RING + pn * kSlotBytes, &q_map, bar(B_QFULL), pn * 64, g.r * p.H);
+                    tma_load_2d(sbase + OFF_RING + pn * kQPanelBytes, &q_map, bar(B_QFULL), pn * 64, g.r * p.H);
                 tma_load_2d(sbase + OFF_QROPE, &q_map, bar(B_QFULL), 8 * 64, g.r * p.H);
-                int issued_n = 0;  // panels issued
+                int issued = 0;  // K panels issued
                 bool ok = true;
                 for (int gi = 0; gi < ngroups && ok; ++gi) {
-                    const int pa = 2 * gi, pbp = 2 * gi + 1;
-                    const bool two = pbp < npages;
-                    const int ya = page_row(p, g.b, g.page0 + pa, true);
-                    const int yb = two ? page_row(p, g.b, g.page0 + pbp, true) : 0;
-                    const int pf = 2 * (gi + kPrefetchGroups);  // prefetch one group further
-                    for (int pg = pf; pg < min(npages, pf + 2); ++pg) {
-                        const int y = page_row(p, g.b, g.page0 + pg, false);
-                        for (int pn = 0; pn < 9; ++pn) tma_prefetch_l2_2d(&kv_map, pn * 64, y);
-                    }
+                    int y[kPPG];
+                    const int np = min(kPPG, npages - kPPG * gi);
+                    for (int q = 0; q < np; ++q) y[q] = page_row(p, g.b, g.page0 + kPPG * gi + q);
                     for (int pn = 0; pn < 9; ++pn) {
-                        int slot, k;
-                        ring_pos(gi, pn, slot, k);
-                        if (k > 0)
-                            ok = wait_bar(bar(B_SLOTEMPTY + slot), (k - 1) & 1, abort, ds);
-                        else if (slot < 8)
-                            ok = wait_bar(bar(B_QREADY), 0, abort, ds);  // Q's panel moved out
+                        const int m = 9 * gi + pn, slot = m % kSlots, k = m / kSlots;
+                        ok = k == 0 ? wait_bar(bar(B_QREADY), 0, abort, ds)  // Q's panels moved out
+                                    : wait_bar(bar(B_SLOTEMPTY + slot), (k - 1) & 1, abort, ds);
                         if (!ok) break;
                         const uint32_t full = bar(B_SLOTFULL + slot);
                         const uint32_t dst = sbase + OFF_RING + slot * kSlotBytes;
-                        bar_arrive_expect_tx(full, (two ? 2 : 1) * kPageBox);
-                        tma_load_2d(dst, &kv_map, full, pn * 64, ya);
-                        if (two) tma_load_2d(dst + kPageBox, &kv_map, full, pn * 64, yb);
-                        ++issued_n;
+                        bar_arrive_expect_tx(full, np * kPageBox);
+                        for (int q = 0; q < np; ++q) tma_load_2d(dst + q * kPageBox, &kv_map, full, pn * 64, y[q]);
+                        ++issued;
                     }
                 }
                 if (*abort) {  // let the copies in flight land before the CTA can exit
                     volatile int dummy = 0;
                     wait_bar(bar(B_QFULL), 0, &dummy, nullptr);
-                    for (int n = (issued_n > kSlots ? issued_n - kSlots : 0); n < issued_n; ++n) {
-                        int slot, k;
-                        ring_pos(n / 9, n % 9, slot, k);
+                    for (int m = (issued > kSlots ? issued - kSlots : 0); m < issued; ++m) {
                         dummy = 0;
-                        wait_bar(bar(B_SLOTFULL + slot), k & 1, &dummy, nullptr);
+                        wait_bar(bar(B_SLOTFULL + m % kSlots), (m / kSlots) & 1, &dummy, nullptr);
                     }
                 }
             }
         } else if (warp == 1) {
             if (lane == 0 && npages > 0) {
-                int done_n = 0;
+                int done = 0;
                 bool ok = wait_bar(bar(B_QREADY), 0, abort, ds);
+                if (ok) tc_fence_after();
                 for (int gi = 0; gi < ngroups && ok; ++gi) {
-                    const int sb = gi & 1, us = gi >> 1;
-                    if (us > 0 && !(ok = wait_bar(bar(B_SEMPTY + sb), (us - 1) & 1, abort, ds))) break;
-                    const uint32_t d = tmem + kSCol + 128u * sb;
-                    for (int pn = 0; pn < 9; ++pn) {
-                        int slot, k;
-                        ring_pos(gi, pn, slot, k);
-                        if (!(ok = wait_bar(bar(B_SLOTFULL + slot), k & 1, abort, ds))) break;
+                    if (gi > 0) {  // the softmax warps have read the previous S out of TMEM
+                        if (!(ok = wait_bar(bar(B_SEMPTY), (gi - 1) & 1, abort, ds))) break;
                         tc_fence_after();
+                    }
+                    const uint32_t d = tmem + kSCol;
+                    for (int pn = 0; pn < 9; ++pn) {
+                        const int m = 9 * gi + pn, slot = m % kSlots, k = m / kSlots;
+                        // TMA-written operands are ordered by the barrier itself: no tcgen05 fence
+                        if (!(ok = wait_bar(bar(B_SLOTFULL + slot), k & 1, abort, ds))) break;
                         const uint32_t kb = sbase + OFF_RING + slot * kSlotBytes;
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -289,22 +265,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             }
                         }
                         mma_commit(bar(B_SLOTEMPTY + slot));
-                        ++done_n;
+                        ++done;
                     }
-                    if (ok) mma_commit(bar(B_SFULL + sb));
+                    if (ok) mma_commit(bar(B_SFULL));
                 }
                 volatile int dummy = 0;  // drain: the last commits have landed before teardown
-                for (int n = (done_n > kSlots ? done_n - kSlots : 0); n < done_n; ++n) {
-                    int slot, k;
-                    ring_pos(n / 9, n % 9, slot, k);
+                for (int m = (done > kSlots ? done - kSlots : 0); m < done; ++m) {
                     dummy = 0;
-                    wait_bar(bar(B_SLOTEMPTY + slot), k & 1, &dummy, nullptr);
+                    wait_bar(bar(B_SLOTEMPTY + m % kSlots), (m / kSlots) & 1, &dummy, nullptr);
                 }
             }
         } else {
             // ------------------------- softmax warps (256 threads) -------------------------
-            const int half = (warp - 2) >> 2;              // page of the group this warp owns
-            const int row = 32 * (warp & 3) + lane;        // head
+            const int half = (warp - 2) >> 2;            // pages 2 half, 2 half + 1 of each group
+            const int row = 32 * (warp & 3) + lane;      // head
             const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
             const bool live = row < p.H;
             float* mx = reinterpret_cast<float*>(smem + OFF_MX);
@@ -318,7 +292,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 8; ++c) {
                         uint4 x = make_uint4(0, 0, 0, 0);
                         if (live && okq)
-                            x = *reinterpret_cast<const uint4*>(smem + OFF_RING + pn * kSlotBytes + row * 128 +
+                            x = *reinterpret_cast<const uint4*>(smem + OFF_RING + pn * kQPanelBytes + row * 128 +
                                                                 ((c ^ (row & 7)) << 4));
                         v[4 * c] = x.x;
                         v[4 * c + 1] = x.y;
@@ -345,32 +319,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t pbuf_remote = map_to_rank(sbase + OFF_PB, 1);
             const uint32_t pfull_remote = map_to_rank(bar(B_PFULL), 1);
             for (int gi = 0; gi < ngroups; ++gi) {
-                const int sb = gi & 1, us = gi >> 1;
-                const int page = 2 * gi + half;
-                const int valid = valid_rows(g, page);
                 // No early exit from this loop: all 256 threads must pass the same named barriers
                 // (which cannot time out); after an abort the waits return at once and the work
                 // is skipped.
-                const bool okS = warp_wait(bar(B_SFULL + sb), us & 1, abort, ds);
-                uint32_t s0[32], s1[32];
+                const bool okS = warp_wait(bar(B_SFULL), gi & 1, abort, ds);
+                uint32_t s[4][32];
                 if (okS) {
                     tc_fence_after();
-                    const uint32_t scol = tmem + lane_base + kSCol + 128u * sb + 64u * half;
-                    tmem_ld32(scol, s0);
-                    tmem_ld32(scol + 32u, s1);
+                    const uint32_t scol = tmem + lane_base + kSCol + 128u * half;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld32(scol + 32u * c, s[c]);
                     tmem_wait_ld();
                     tc_fence_before();
-                    bar_arrive(bar(B_SEMPTY + sb));
+                    bar_arrive(bar(B_SEMPTY));
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) s0[c] = s1[c] = __float_as_uint(-CUDART_INF_F);
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) s[c][j] = __float_as_uint(-CUDART_INF_F);
                 }
+                const int pg0 = kPPG * gi + 2 * half;  // first of this half's two pages
+                const int valid0 = valid_rows(g, pg0), valid1 = valid_rows(g, pg0 + 1);
                 float lm = -CUDART_INF_F;
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    if (c >= valid) s0[c] = __float_as_uint(-CUDART_INF_F);
-                    if (c + 32 >= valid) s1[c] = __float_as_uint(-CUDART_INF_F);
-                    lm = fmaxf(lm, fmaxf(__uint_as_float(s0[c]), __uint_as_float(s1[c])));
+                for (int c = 0; c < 4; ++c) {
+                    const int v = c < 2 ? valid0 - 32 * c : valid1 - 32 * (c - 2);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (j >= v) s[c][j] = __float_as_uint(-CUDART_INF_F);
+                        lm = fmaxf(lm, __uint_as_float(s[c][j]));
+                    }
                 }
                 mx[half * 128 + row] = lm;
                 named_bar(kBarMax, 256);
@@ -381,42 +359,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     alpha = fast_exp2(m_run - mt);  // 0 on the first group (m_run = -inf)
                     m_run = mt;
                 }
-                uint32_t pk[32];
-                float sum = 0.f, sum_t = 0.f;
+                l_run *= alpha;
+                lt_run *= alpha;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float a0 = fast_exp2(fmaf(__uint_as_float(s0[2 * c]), sl2, -m_run));
-                    const float a1 = fast_exp2(fmaf(__uint_as_float(s0[2 * c + 1]), sl2, -m_run));
-                    const float b0 = fast_exp2(fmaf(__uint_as_float(s1[2 * c]), sl2, -m_run));
-                    const float b1 = fast_exp2(fmaf(__uint_as_float(s1[2 * c + 1]), sl2, -m_run));
-                    pk[c] = pack_bf16x2(a0, a1);
-                    pk[16 + c] = pack_bf16x2(b0, b1);
-                    sum_t += (a0 + a1) + (b0 + b1);
-                    sum += (bf16_lo_f(pk[c]) + bf16_hi_f(pk[c])) + (bf16_lo_f(pk[16 + c]) + bf16_hi_f(pk[16 + c]));
-                }
-                l_run = l_run * alpha + sum;
-                lt_run = lt_run * alpha + sum_t;
-                const bool exists = page < npages;
-                const int stg = page % kStageBufs, ust = page / kStageBufs;
-                bool ok = okS;
-                if (ok && exists && ust > 0) ok = warp_wait<true>(bar(B_STAGEFREE + stg), (ust - 1) & 1, abort, ds);
-                uint8_t* sbuf = smem + OFF_STAGE + stg * kPBufStride;
-                if (exists && ok) {
+                for (int q = 0; q < 2; ++q) {
+                    const int page = pg0 + q;
+                    uint32_t pk[32];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(sbuf + row * 128 + ((c ^ (row & 7)) << 4)) =
-                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                    reinterpret_cast<float*>(sbuf + kPBytes)[row] = half == 0 ? alpha : 1.f;
-                    fence_proxy_async_cta();
+                    for (int c = 0; c < 16; ++c) {
+                        const float a0 = fast_exp2(fmaf(__uint_as_float(s[2 * q][2 * c]), sl2, -m_run));
+                        const float a1 = fast_exp2(fmaf(__uint_as_float(s[2 * q][2 * c + 1]), sl2, -m_run));
+                        const float b0 = fast_exp2(fmaf(__uint_as_float(s[2 * q + 1][2 * c]), sl2, -m_run));
+                        const float b1 = fast_exp2(fmaf(__uint_as_float(s[2 * q + 1][2 * c + 1]), sl2, -m_run));
+                        pk[c] = pack_bf16x2(a0, a1);
+                        pk[16 + c] = pack_bf16x2(b0, b1);
+                        lt_run += (a0 + a1) + (b0 + b1);
+                        l_run += (bf16_lo_f(pk[c]) + bf16_hi_f(pk[c])) + (bf16_lo_f(pk[16 + c]) + bf16_hi_f(pk[16 + c]));
+                    }
+                    if (page < npages && okS) {
+                        const int stg = page % kPBufs, ust = page / kPBufs;
+                        if (ust > 0 && !warp_wait<true>(bar(B_STAGEFREE + stg), (ust - 1) & 1, abort, ds)) continue;
+                        uint8_t* sbuf = smem + OFF_STAGE + stg * kPBufStride;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4*>(sbuf + row * 128 + ((c ^ (row & 7)) << 4)) =
+                                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                        // every row's alpha rides with the group's first page
+                        if (half == 0 && q == 0) reinterpret_cast<float*>(sbuf + kPBytes)[row] = alpha;
+                        fence_proxy_async_cta();
+                    }
                 }
-                // every row's alpha is shipped with the group's first page; the flag tells CTA 1
-                // whether any of them differs from 1
                 const bool any = named_bar_or(kBarOr, 256, resc && gi > 0);
-                if (tid == 64 && !*abort) {
-                    for (int q = 0; q < 2; ++q) {
-                        const int pg = 2 * gi + q;
+                if (tid == 64 && !*abort) {  // one thread ships the group's pages
+                    for (int q = 0; q < kPPG; ++q) {
+                        const int pg = kPPG * gi + q;
                         if (pg >= npages) break;
-                        uint8_t* b = smem + OFF_STAGE + (pg % kStageBufs) * kPBufStride;
+                        uint8_t* b = smem + OFF_STAGE + (pg % kPBufs) * kPBufStride;
                         *reinterpret_cast<uint32_t*>(b + kPBytes + 512) = (q == 0 && any) ? 1u : 0u;
                         fence_proxy_async_cta();
                         const int pbi = pg % kPBufs, upb = pg / kPBufs;
@@ -446,11 +424,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int pg = (npages > kPBufs ? npages - kPBufs : 0); pg < npages; ++pg) {
                         volatile int dummy = 0;
                         wait_bar<true>(bar(B_PEMPTY + pg % kPBufs), (pg / kPBufs) & 1, *abort ? &dummy : abort, ds);
-                    }
-                    for (int pg = (npages > kStageBufs ? npages - kStageBufs : 0); pg < npages; ++pg) {
-                        volatile int dummy = 0;
-                        wait_bar<true>(bar(B_STAGEFREE + pg % kStageBufs), (pg / kStageBufs) & 1,
-                                       *abort ? &dummy : abort, ds);
+                        dummy = 0;
+                        wait_bar<true>(bar(B_STAGEFREE + pg % kPBufs), (pg / kPBufs) & 1, *abort ? &dummy : abort,
+                                       ds);
                     }
                 }
             }
@@ -466,7 +442,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (kv > 0 && !wait_bar(bar(B_VEMPTY + st), (kv - 1) & 1, abort, ds)) break;
                     const uint32_t full = bar(B_VFULL + st);
                     bar_arrive_expect_tx(full, kVStageBytes);
-                    const int y = page_row(p, g.b, g.page0 + i, false);
+                    const int y = page_row(p, g.b, g.page0 + i);
                     const uint32_t dst = sbase + OFF_V + st * kVStageBytes;
 #pragma unroll
                     for (int pn = 0; pn < 8; ++pn) tma_load_2d(dst + pn * kPageBox, &kv_map, full, pn * 64, y);
@@ -480,35 +456,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
         } else if (warp == 1) {
+            // MMA thread: one wait per page (READY), then the page's 8 N=256 MMAs and commits
             if (lane == 0) {
-                volatile uint32_t* req_word = reinterpret_cast<volatile uint32_t*>(smem + OFF_REQ);
-                int n_req = 0, n_ostep = 0, done = 0;
-                bool ok = true;
-                for (int i = 0; i < npages && ok; ++i) {
-                    const int st = i % kVStages, kv = i / kVStages, pb = i % kPBufs, up = i / kPBufs;
-                    ok = wait_bar(bar(B_VFULL + st), kv & 1, abort, ds) &&
-                         wait_bar(bar(B_PFULL + pb), up & 1, abort, ds);
-                    if (!ok) break;
-                    // the staging buffer in CTA 0 has been copied out: let it be reused
-                    bar_arrive_remote(bar(B_STAGEFREE + i % kStageBufs), 0);
-                    const uint8_t* pmsg = smem + OFF_PB + pb * kPBufStride;
-                    const bool fix = i > 0 && *reinterpret_cast<const volatile uint32_t*>(pmsg + kPBytes + 512) != 0;
-                    const int valid = valid_rows(g, i);
-                    if (fix || valid < kPage) {
-                        if (fix) {  // the rescale must see every earlier PV product in O
-                            mma_commit(bar(B_OSTEP));
-                            ok = wait_bar(bar(B_OSTEP), n_ostep & 1, abort, ds);
-                            ++n_ostep;
-                            if (!ok) break;
-                        }
-                        *req_word = (fix ? REQ_FIX : 0u) | (valid < kPage ? REQ_TAIL : 0u) | ((uint32_t)pb << 4) |
-                                    ((uint32_t)st << 8) | ((uint32_t)valid << 12);
-                        bar_arrive(bar(B_REQ));
-                        ok = wait_bar(bar(B_DONE), n_req & 1, abort, ds);
-                        ++n_req;
-                        if (!ok) break;
-                    }
-                    tc_fence_after();
+                int done = 0;
+                for (int i = 0; i < npages; ++i) {
+                    const int st = i % kVStages, pb = i % kPBufs;
+                    if (!wait_bar(bar(B_READY + pb), (i / kPBufs) & 1, abort, ds)) break;
+                    tc_fence_after();  // after a rescale by the helper warps' tcgen05.st
                     const uint32_t vb = sbase + OFF_V + st * kVStageBytes;
                     const uint32_t pbuf = sbase + OFF_PB + pb * kPBufStride;
 #pragma unroll
@@ -522,17 +476,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     mma_commit(bar(B_VEMPTY + st));
                     mma_commit_multicast(bar(B_PEMPTY + pb), (uint16_t)0x1);
-                    bar_arrive_expect_tx(bar(B_PFULL + pb), kPMsgBytes);  // armed for its next message
+                    mma_commit(bar(B_OSTEP));
                     done = i + 1;
                 }
-                uint32_t end = REQ_END;
-                if (done > 0) {
-                    mma_commit(bar(B_OSTEP));  // completes when the last PV product is in O
-                    end |= ((uint32_t)(n_ostep & 1) << 20) | (ok && done == npages ? REQ_HAS_O : 0u);
-                    ++n_ostep;
-                }
-                *req_word = end;
-                bar_arrive(bar(B_REQ));
                 volatile int dummy = 0;  // drain the V-ring commits before teardown
                 for (int i = (done > kVStages ? done - kVStages : 0); i < done; ++i) {
                     dummy = 0;
@@ -540,22 +486,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
         } else if (warp < 6) {
-            // ------------------ helper warps: rescale, tail zeroing, epilogue ------------------
+            // ------------- helper warps: P / V arrival, rescale, tail zeroing, epilogue -------------
             const int row = 32 * (warp & 3) + lane;
             const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
             const int ctid = tid - 64;  // 0..127
-            uint32_t req = REQ_END;
-            for (int k = 0;; ++k) {
-                if (!warp_wait(bar(B_REQ), k & 1, abort, ds)) {
-                    req = REQ_END;
-                    break;
+            int pages_ready = 0;
+            for (int i = 0; i < npages; ++i) {
+                const int st = i % kVStages, kv = i / kVStages, pb = i % kPBufs, up = i / kPBufs;
+                if (!warp_wait(bar(B_PFULL + pb), up & 1, abort, ds)) break;
+                if (ctid == 0) {
+                    // the staging buffer in CTA 0 has been copied out; re-arm for the next message
+                    bar_arrive_remote(bar(B_STAGEFREE + pb), 0);
+                    bar_arrive_expect_tx(bar(B_PFULL + pb), kPMsgBytes);
                 }
-                req = *reinterpret_cast<volatile uint32_t*>(smem + OFF_REQ);
-                if (req & REQ_END) break;
-                const int pb = (req >> 4) & 15, st = (req >> 8) & 15, valid = (req >> 12) & 255;
-                if (req & REQ_FIX) {
+                const uint8_t* pmsg = smem + OFF_PB + pb * kPBufStride;
+                const bool fix = i > 0 && *reinterpret_cast<const volatile uint32_t*>(pmsg + kPBytes + 512) != 0;
+                const int valid = valid_rows(g, i);
+                if (fix) {  // O must hold every earlier PV product before it is rescaled
+                    if (!warp_wait(bar(B_OSTEP), (i - 1) & 1, abort, ds)) break;
                     tc_fence_after();
-                    const float a = reinterpret_cast<volatile float*>(smem + OFF_PB + pb * kPBufStride + kPBytes)[row];
+                    const float a = reinterpret_cast<const volatile float*>(pmsg + kPBytes)[row];
 #pragma unroll 1
                     for (int c = 0; c < kL / 32; ++c) {
                         uint32_t v[32];
@@ -567,7 +517,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();
                 }
-                if (req & REQ_TAIL) {  // zero V rows [valid, 64) of all 8 panels of the stage
+                if (!warp_wait(bar(B_VFULL + st), kv & 1, abort, ds)) break;
+                if (valid < kPage) {  // zero V rows [valid, 64) of all 8 panels of the stage
                     const uint32_t vb = OFF_V + st * kVStageBytes;
                     const int chunks = (kPage - valid) * 8 * 8;
                     for (int q = ctid; q < chunks; q += 128) {
@@ -578,17 +529,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     fence_proxy_async_cta();
                 }
                 tc_fence_before();
-                bar_arrive(bar(B_DONE));
+                bar_arrive(bar(B_READY + pb));
+                pages_ready = i + 1;
             }
             // epilogue
-            const bool has_o = (req & REQ_HAS_O) != 0;
+            const bool has_o = npages > 0 && pages_ready == npages && !*abort;
             wait_bar<true>(bar(B_STATS), 0, abort, ds);
-            if (has_o) wait_bar(bar(B_OSTEP), (req >> 20) & 1, abort, ds);
+            const bool o_ok = has_o && wait_bar(bar(B_OSTEP), (npages - 1) & 1, abort, ds);
             tc_fence_after();
             const float m = reinterpret_cast<volatile float*>(smem + OFF_STAT_M)[row];
             const float l = reinterpret_cast<volatile float*>(smem + OFF_STAT_L)[row];
             const float lt = reinterpret_cast<volatile float*>(smem + OFF_STAT_LT)[row];
-            const bool empty = !has_o || !(l > 0.f);
+            const bool use_o = __all_sync(0xffffffffu, o_ok);
+            const bool empty = !use_o || !(l > 0.f);
             const float inv = empty ? 0.f : 1.f / l;
             const float lse_v = empty ? -CUDART_INF_F : (m + log2f(lt)) * 0.6931471805599453f;
             const bool live = row < p.H;
@@ -607,7 +560,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int c = 0; c < kL / 32; ++c) {
                 uint32_t v[32];
-                if (has_o) {
+                if (use_o) {
                     tmem_ld32(tmem + lane_base + 32u * c, v);
                     tmem_wait_ld();
                 } else {
