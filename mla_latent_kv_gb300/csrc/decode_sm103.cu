@@ -92,14 +92,13 @@ enum : int {
     B_QFULL = 10,       // CTA0: Q landed in shared memory (TMA tx)
     B_QREADY = 11,      // CTA0: Q latent dims moved to TMEM, ring free for K (256)
     B_STAGEFREE = 12,   // [4] CTA0: staging buffer copied out (arrive from CTA1)
-    B_PEMPTY = 16,      // [4] CTA0: CTA1's P buffer consumed by its PV MMA (multicast commit)
+    B_PEMPTY = 16,      // [4] both CTAs: PV MMA of the page in P buffer b completed (multicast commit)
     B_VFULL = 20,       // [2] CTA1: V stage landed
     B_VEMPTY = 22,      // [2] CTA1: V stage consumed
     B_PFULL = 24,       // [4] CTA1: P message landed (bulk copy tx)
     B_READY = 28,       // [4] CTA1: page ready for its PV MMA (128 helper threads)
-    B_OSTEP = 32,       // CTA1: PV MMAs of a page completed (one phase per page)
-    B_STATS = 33,       // CTA1: final row statistics written by CTA0 (one cluster-scope arrive)
-    B_COUNT = 34
+    B_STATS = 32,       // CTA1: final row statistics written by CTA0 (one cluster-scope arrive)
+    B_COUNT = 33
 };
 constexpr int OFF_TMEM = 512;
 constexpr int OFF_ABORT = 516;
@@ -461,6 +460,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 int done = 0;
                 for (int i = 0; i < npages; ++i) {
                     const int st = i % kVStages, pb = i % kPBufs;
+                    // V and P were written by the async proxy (TMA / bulk copy): the MMA thread
+                    // observes their barriers itself; READY adds the helpers' rescale / zeroing.
+                    if (!wait_bar(bar(B_VFULL + st), (i / kVStages) & 1, abort, ds)) break;
+                    if (!wait_bar(bar(B_PFULL + pb), (i / kPBufs) & 1, abort, ds)) break;
                     if (!wait_bar(bar(B_READY + pb), (i / kPBufs) & 1, abort, ds)) break;
                     tc_fence_after();  // after a rescale by the helper warps' tcgen05.st
                     const uint32_t vb = sbase + OFF_V + st * kVStageBytes;
@@ -475,8 +478,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                     }
                     mma_commit(bar(B_VEMPTY + st));
-                    mma_commit_multicast(bar(B_PEMPTY + pb), (uint16_t)0x1);
-                    mma_commit(bar(B_OSTEP));
+                    // P buffer pb is free again (CTA 0) and O holds page i (helper warps, CTA 1).
+                    // One barrier per P buffer keeps every waiter within one phase of it: a
+                    // page's P only arrives after the PV of the page four earlier completed.
+                    mma_commit_multicast(bar(B_PEMPTY + pb), (uint16_t)0x3);
                     done = i + 1;
                 }
                 volatile int dummy = 0;  // drain the V-ring commits before teardown
@@ -503,7 +508,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const bool fix = i > 0 && *reinterpret_cast<const volatile uint32_t*>(pmsg + kPBytes + 512) != 0;
                 const int valid = valid_rows(g, i);
                 if (fix) {  // O must hold every earlier PV product before it is rescaled
-                    if (!warp_wait(bar(B_OSTEP), (i - 1) & 1, abort, ds)) break;
+                    if (!warp_wait(bar(B_PEMPTY + (i - 1) % kPBufs), ((i - 1) / kPBufs) & 1, abort, ds)) break;
                     tc_fence_after();
                     const float a = reinterpret_cast<const volatile float*>(pmsg + kPBytes)[row];
 #pragma unroll 1
@@ -535,7 +540,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // epilogue
             const bool has_o = npages > 0 && pages_ready == npages && !*abort;
             wait_bar<true>(bar(B_STATS), 0, abort, ds);
-            const bool o_ok = has_o && wait_bar(bar(B_OSTEP), (npages - 1) & 1, abort, ds);
+            const bool o_ok =
+                has_o && wait_bar(bar(B_PEMPTY + (npages - 1) % kPBufs), ((npages - 1) / kPBufs) & 1, abort, ds);
             tc_fence_after();
             const float m = reinterpret_cast<volatile float*>(smem + OFF_STAT_M)[row];
             const float l = reinterpret_cast<volatile float*>(smem + OFF_STAT_L)[row];
