@@ -169,6 +169,30 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
 mla_status mla_out_proj(const void* o_latent, mla_dtype in_dtype, const void* W_UV, void* o,
                         mla_dtype out_dtype, int T, int H, mla_stream_t stream);
 
+/*
+ * mla_decode without a workspace argument, for callers that cannot allocate device memory when
+ * they decode: serving loops that run under a fixed device-memory budget with every buffer made
+ * at start-up, host runtimes that forbid device allocations after initialisation, and call paths
+ * that cannot carry a workspace pointer down to the attention call. (The pages have no
+ * counterpart of this call; it only changes where the split-KV scratch lives.)
+ *
+ * Same arguments, meaning and results as mla_decode, minus workspace / workspace_bytes. The
+ * split-KV partials live in one file-scope device array of mla_decode_noalloc_max_workspace_bytes()
+ * bytes (64 MiB), held on every device that uses it until the process exits. The first call on a
+ * device looks up the array's device address (once per device, with that device current); make
+ * that first call before any stream capture. Split plans that need more than the array holds are
+ * refused with MLA_ERR_WORKSPACE_TOO_SMALL before any launch. Nothing here calls cudaMalloc,
+ * cudaFree or any allocating library routine. All calls share the array: calls whose kernels
+ * overlap on the GPU (e.g. issued on different streams) race on it and must be serialised by
+ * the caller. The array keeps the last call's contents; no result depends on them.
+ */
+size_t mla_decode_noalloc_max_workspace_bytes(void);
+mla_status mla_decode_noalloc(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype, int64_t num_blocks,
+                              const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                              int max_seq_len, int B, int Sq, int H, float scale, int num_splits,
+                              void* o_latent, mla_dtype o_dtype, float* lse, int32_t* dev_status,
+                              mla_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -60,6 +60,11 @@ def lib() -> ctypes.CDLL:
         l.mla_decode.restype = i32
         l.mla_decode.argtypes = [vp, vp, i32, i64, vp, i32, vp, i32, i32, i32, i32, f32, i32, vp, sz,
                                  vp, i32, vp, vp, vp]
+        l.mla_decode_noalloc_max_workspace_bytes.restype = sz
+        l.mla_decode_noalloc_max_workspace_bytes.argtypes = []
+        l.mla_decode_noalloc.restype = i32
+        l.mla_decode_noalloc.argtypes = [vp, vp, i32, i64, vp, i32, vp, i32, i32, i32, i32, f32, i32, vp, i32,
+                                         vp, vp, vp]
         l.mla_out_proj.restype = i32
         l.mla_out_proj.argtypes = [vp, i32, vp, vp, i32, i32, i32, vp]
         _lib = l
@@ -151,6 +156,31 @@ def decode(q, kv_cache, block_table, seq_lens, max_seq_len, scale, kv_dtype=KV_B
                             block_table.shape[1], _p(seq_lens), int(max_seq_len), B, Sq, H, float(scale),
                             int(S), _p(workspace), ws_bytes, _p(o_latent), o_dtype, _p(lse), _p(dev_status),
                             _stream(stream)))
+    return o_latent, lse
+
+
+def noalloc_max_workspace_bytes() -> int:
+    return int(lib().mla_decode_noalloc_max_workspace_bytes())
+
+
+def decode_noalloc(q, kv_cache, block_table, seq_lens, max_seq_len, scale, kv_dtype=KV_BF16, num_splits=0,
+                   o_latent=None, o_dtype=DT_F32, lse=None, dev_status=None, stream=None, num_blocks=None):
+    """decode() through mla_decode_noalloc: the split-KV scratch is the library's own fixed device
+    array, so no workspace is passed (outputs are still made here when not given)."""
+    import torch
+    B, Sq, H = q.shape[0], q.shape[1], q.shape[2]
+    dev = q.device
+    if num_blocks is None:
+        num_blocks = kv_cache.numel() * kv_cache.element_size() // (PAGE * row_bytes(kv_dtype))
+    if o_latent is None:
+        o_latent = torch.empty((B, Sq, H, L), dtype=torch.float32 if o_dtype == DT_F32 else torch.bfloat16,
+                               device=dev)
+    if lse is None:
+        lse = torch.empty((B, Sq, H), dtype=torch.float32, device=dev)
+    _check(lib().mla_decode_noalloc(_p(q), _p(kv_cache), kv_dtype, int(num_blocks), _p(block_table),
+                                    block_table.shape[1], _p(seq_lens), int(max_seq_len), B, Sq, H, float(scale),
+                                    int(num_splits), _p(o_latent), o_dtype, _p(lse), _p(dev_status),
+                                    _stream(stream)))
     return o_latent, lse
 
 

@@ -50,6 +50,9 @@ __host__ __device__ inline void split_range(int n, int S, int s, int* j0, int* j
     *j1 = e < n ? e : n;
 }
 
+// Record an error for mla_last_error_detail() and return `st` (printf-style message).
+mla_status set_error(mla_status st, const char* fmt, ...);
+
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);

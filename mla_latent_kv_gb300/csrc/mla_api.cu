@@ -47,6 +47,16 @@ int device_sm_count() {
 
 }  // namespace
 
+namespace mla {
+mla_status set_error(mla_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_detail, sizeof g_detail, fmt, ap);
+    va_end(ap);
+    return st;
+}
+}  // namespace mla
+
 extern "C" {
 
 const char* mla_status_string(mla_status s) {
