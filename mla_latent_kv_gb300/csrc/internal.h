@@ -53,13 +53,12 @@ __host__ __device__ inline void split_range(int n, int S, int s, int* j0, int* j
 // Record an error for mla_last_error_detail() and return `st` (printf-style message).
 mla_status set_error(mla_status st, const char* fmt, ...);
 
-cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);
-cudaError_t launch_absorb_simt(const uint16_t* q_nope, int64_t snt, int64_t snh, const uint16_t* q_pe,
-                               int64_t spt, int64_t sph, const uint16_t* w_uk_t, uint16_t* q_out,
-                               int T, int H, cudaStream_t s);
-cudaError_t launch_out_proj_simt(const void* o_latent, int in_dtype, const uint16_t* w_uv, void* o,
-                                 int out_dtype, int T, int H, cudaStream_t s);
+cudaError_t launch_absorb_sm103(const uint16_t* q_nope, int64_t snt, int64_t snh, const uint16_t* q_pe,
+                                int64_t spt, int64_t sph, const uint16_t* w_uk_t, uint16_t* q_out, int T, int H,
+                                cudaStream_t s);
+cudaError_t launch_out_proj_sm103(const void* o_latent, int in_dtype, const uint16_t* w_uv, void* o,
+                                  int out_dtype, int T, int H, cudaStream_t s);
 
 }  // namespace mla

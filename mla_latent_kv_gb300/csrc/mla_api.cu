@@ -141,7 +141,7 @@ mla_status mla_absorb_q(const void* q_nope, int64_t snt, int64_t snh, const void
         return fail(MLA_ERR_UNSUPPORTED, "mla_absorb_q: strides must be non-negative multiples of 8");
     if (snh < mla::kP && H > 1)
         return fail(MLA_ERR_INVALID_ARG, "mla_absorb_q: q_nope head stride %lld < 128", (long long)snh);
-    cudaError_t e = mla::launch_absorb_simt((const uint16_t*)q_nope, snt, snh, (const uint16_t*)q_pe, spt,
+    cudaError_t e = mla::launch_absorb_sm103((const uint16_t*)q_nope, snt, snh, (const uint16_t*)q_pe, spt,
                                            sph, (const uint16_t*)W_UK_T, (uint16_t*)q_out, T, H,
                                            (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "mla_absorb_q launch");
@@ -237,7 +237,7 @@ mla_status mla_out_proj(const void* o_latent, mla_dtype in_dtype, const void* W_
     if (!o_latent || !W_UV || !o) return fail(MLA_ERR_INVALID_ARG, "mla_out_proj: null pointer");
     if (!aligned16(o_latent) || !aligned16(W_UV) || !aligned16(o))
         return fail(MLA_ERR_UNSUPPORTED, "mla_out_proj: pointers must be 16-byte aligned");
-    cudaError_t e = mla::launch_out_proj_simt(o_latent, in_dtype, (const uint16_t*)W_UV, o, out_dtype, T, H,
+    cudaError_t e = mla::launch_out_proj_sm103(o_latent, in_dtype, (const uint16_t*)W_UV, o, out_dtype, T, H,
                                               (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "mla_out_proj launch");
     return ok();

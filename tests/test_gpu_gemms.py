@@ -68,6 +68,10 @@ def test_out_proj(T, H, in_bf16, out_bf16):
     extra = float(np.abs(ref).max()) * 2.0 ** -9 if out_bf16 else 0.0
     assert np.abs(got - ref).max() <= TOL_MAX_ABS + extra
     assert rel_l2(got, ref) <= TOL_REL_L2
+    if not out_bf16:
+        # fp32 accumulation of 512 products whose fp32 operand is carried as bf16 hi + lo: the
+        # result is close to exact, far inside the decode tolerance
+        assert np.abs(got - ref).max() <= 1e-4 * max(1.0, float(np.abs(ref).max()))
 
 
 @pytest.mark.parametrize("B,Sq,H,lens,splits", [(2, 1, 16, [128, 300], 0), (3, 2, 128, [1, 65, 400], 3),
