@@ -115,8 +115,9 @@ size_t mla_decode_workspace_bytes(int B, int Sq, int H, int num_splits);
  *           in which case q_out[..., 512:576] is left untouched
  *   W_UK_T  bf16 [H, 128, 512] contiguous (vLLM's W_UK.permute(1, 2, 0))
  *   q_out   bf16 [T, H, 576] contiguous; must not overlap the inputs
- * Strides are in elements and must be multiples of 8 (16-byte rows for TMA); all pointers
- * 16-byte aligned. 1 <= H <= 128, T >= 0 (T == 0 launches nothing).
+ * Strides are in elements and must be multiples of 8 (16-byte rows for TMA); q_nope_stride_t
+ * must be non-zero when T > 1 and q_nope_stride_h >= 128 when H > 1. All pointers 16-byte
+ * aligned. 1 <= H <= 128, T >= 0 (T == 0 launches nothing).
  */
 mla_status mla_absorb_q(const void* q_nope, int64_t q_nope_stride_t, int64_t q_nope_stride_h,
                         const void* q_pe, int64_t q_pe_stride_t, int64_t q_pe_stride_h,

@@ -1,5 +1,5 @@
 // gemm_sm103.cu -- the two per-head batched GEMMs of the absorbed MLA path on the 5th-generation
-// tensor cores (tcgen05 + TMEM accumulators, weights staged by TMA).
+// tensor cores (tcgen05 + TMEM accumulators, all operands staged by TMA).
 //
 //   absorb:   q[t, h, 0:512]   = q_nope[t, h, :] . W_UK_T[h]      (K = 128, M = 512)
 //             q[t, h, 512:576] = q_pe[t, h, :]                      (copied, fused concat)
@@ -10,24 +10,28 @@
 //
 // Both are D[t, h, m] = sum_k W[h][k][m] * X[t, h, k] with the weights stored [H][K][M] (m
 // fastest) and few tokens T (decode batches). The kernel runs them "swap-AB": the MMA's M side is
-// the weight's m (128 rows per CTA, the full tensor-core height) and its N side is the token
-// count, so a batch of a handful of tokens does not waste a 128-row MMA. A = W[h]^T is read
+// the weight's m (128 rows per work unit, the full tensor-core height) and its N side is the
+// token count, so a batch of a handful of tokens does not waste a 128-row MMA. A = W[h]^T is read
 // MN-major straight from the weight layout; B = X^T is K-major.
 //
-// Work split: one CTA per (128-row m tile, head, tile of up to 128 tokens). K is walked in
-// 64-deep chunks through a ring of shared-memory stages:
-//   warp 4 lane 0  TMA of the weight chunk (two 64 x 64 boxes, 128-byte swizzle) per stage
-//   warps 0-3      load the activation chunk with plain 16-byte loads, convert it to bf16 and
-//                  write it in the swizzled K-major layout the MMA reads; an fp32 activation
-//                  (out_proj's o_latent) is split into bf16 hi + lo parts, x = hi + lo to ~2^-17
-//                  relative, and both are multiplied (two MMAs per K step), so the fp32 input is
-//                  not truncated to bf16
-//   warp 5 lane 0  issues the tcgen05.mma (M = 128, N = token tile, K = 16 per instruction),
-//                  commits each stage back to its producers and, at the end, the accumulator
-//   warps 0-3      epilogue: tcgen05.ld of the fp32 accumulator (lane = m, column = token) and
-//                  the stores to the output (rounded once to bf16 where the output is bf16)
-// The weights (16.8 MB per GEMM at H = 128) are read from HBM once per token tile; the kernel is
-// bound by that stream, not by the tensor cores.
+// A work unit is (128-row m tile, head, tile of up to 128 tokens). The kernel is persistent: one
+// CTA per SM walks units u = blockIdx.x, + gridDim.x, ..., and every role streams across unit
+// boundaries, so the weight stream (16.8 MB per GEMM at H = 128, read once per token tile) never
+// waits for an epilogue:
+//   warp 4 lane 0  TMA producer: per 64-deep K chunk, two 64 x 64 weight boxes and the
+//                  activation box(es) into a ring stage (128-byte swizzle for bf16 operands)
+//   warps 6-9      fp32 activations only (out_proj's o_latent): rewrite each staged fp32 chunk
+//                  in place as bf16 hi + lo panels, x = hi + lo to ~2^-17 relative; both panels
+//                  are multiplied (two MMAs per K step), so the fp32 input is not cut to bf16
+//   warp 5 lane 0  tcgen05.mma (M = 128, N = token tile, K = 16 per instruction) into one of two
+//                  TMEM accumulators, commits each ring stage back to the producer and each
+//                  finished accumulator to the epilogue
+//   warps 0-3      epilogue: tcgen05.ld of the fp32 accumulator (lane = m, column = token) in
+//                  32-token slices, each written (rounded once where the output is bf16) to a
+//                  double-buffered [32 tokens][128 m] shared tile that one thread sends out with
+//                  a TMA store; then frees the accumulator for the unit after next
+//   warps 6-9      bf16 activations (absorb): the fused q_pe copy, off the epilogue's path
+// Every wait is bounded; a CTA that gives up writes NaN to the outputs it owns.
 #include <cuda.h>
 
 #include "internal.h"
@@ -43,74 +47,84 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 192;      // warps 0-3 loaders + epilogue, warp 4 TMA + TMEM, warp 5 MMA
-constexpr int kKChunk = 64;        // K rows per stage
-constexpr int kMaxStages = 4;
-constexpr int kWBox = 64 * 64 * 2; // one 64 (m) x 64 (k) bf16 box = 8 KB
-constexpr int kWStage = 2 * kWBox; // 128 m rows per CTA
+constexpr int kThreads = 320;       // warps 0-3 epilogue, 4 TMA + TMEM, 5 MMA, 6-9 fp32 split
+constexpr int kKChunk = 64;         // K rows per ring stage
+constexpr int kStages = 4;
+constexpr int kWBox = 64 * 64 * 2;  // one 64 (m) x 64 (k) bf16 box = 8 KB
+constexpr int kWStage = 2 * kWBox;  // 128 m rows per unit
+constexpr uint32_t kBarConvert = 1; // named barrier of the fp32-split warps
+constexpr uint32_t kBarEpi = 2;     // named barrier of the epilogue warps
+constexpr int kSlice = 32;          // tokens per epilogue slice (one tcgen05.ld 32x32b.x32)
 
 struct HeadGemmArgs {
-    int T, H, K;
-    int n_tile;          // tokens per CTA: multiple of 16, <= 128
-    int stages;          // ring depth, <= kMaxStages
-    const void* x;       // activations, element (t, h, k) at x[t * x_st + h * x_sh + k]
-    int x_f32;           // 1: fp32 (split into bf16 hi + lo), 0: bf16
-    int64_t x_st, x_sh;
-    void* out;           // element (t, h, m) at out[t * out_st + h * out_sh + m]
+    int T, H, K, M_total;
+    int n_tile;              // tokens per unit: multiple of 16, <= 128
+    int x_f32;               // activations fp32 (split into bf16 hi + lo) or bf16
+    void* out;               // element (t, h, m) at out[t * out_st + h * out_sh + m]
     int out_f32;
     int64_t out_st, out_sh;
-    const uint16_t* q_pe; // absorb only (may be null): copied to out[t, h, 512:576] by m tile 0
+    const uint16_t* q_pe;    // absorb only (may be null): copied to out[t, h, 512:576] by m tile 0
     int64_t pe_st, pe_sh;
 };
 
-__device__ __forceinline__ uint32_t bf16_bits_rn(float x) { return pack_bf16x2(x, 0.f) & 0xffffu; }
+struct Unit {
+    int mt, h, nt;
+};
 
-__device__ __forceinline__ void store_out(const HeadGemmArgs& p, int t, int m, float v) {
-    const int64_t off = (int64_t)t * p.out_st + (int64_t)blockIdx.y * p.out_sh + m;
-    if (p.out_f32)
-        static_cast<float*>(p.out)[off] = v;
-    else
-        static_cast<uint16_t*>(p.out)[off] = (uint16_t)bf16_bits_rn(v);
+__device__ __forceinline__ Unit unit_of(int u, int n_tiles, int m_tiles) {
+    Unit r;
+    r.nt = u % n_tiles;
+    const int rest = u / n_tiles;
+    r.mt = rest % m_tiles;
+    r.h = rest / m_tiles;
+    return r;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    head_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const HeadGemmArgs p) {
+    head_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constant__ CUtensorMap x_map,
+                     const __grid_constant__ CUtensorMap o_map, const HeadGemmArgs p) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[3 * kMaxStages + 1];
+    __shared__ __align__(8) uint64_t bars[3 * kStages + 4];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.y;
-    const int m0 = blockIdx.x * 128;
-    const int n0 = blockIdx.z * p.n_tile;
     const int NT = p.n_tile;
-    const int ST = p.stages;
+    const int n_tiles = (p.T + NT - 1) / NT;
+    const int m_tiles = p.M_total / 128;
+    const int units = n_tiles * m_tiles * p.H;
     const int nchunks = p.K / kKChunk;
-    const uint32_t x_panel = (uint32_t)NT * 128u;  // one 64-deep K-major panel of NT rows
-    const uint32_t stage_bytes = kWStage + (p.x_f32 ? 2u : 1u) * x_panel;
+    const uint32_t x_panel = (uint32_t)NT * 128u;  // one 64-deep bf16 K-major panel of NT rows
+    const uint32_t x_bytes = (p.x_f32 ? 2u : 1u) * x_panel;
+    const uint32_t stage_bytes = kWStage + x_bytes;
+    const uint32_t acc_cols = NT <= 32 ? 32u : (NT <= 64 ? 64u : 128u);
+    const uint32_t out_es = p.out_f32 ? 4u : 2u;
+    const uint32_t slice_bytes = kSlice * 128u * out_es;  // [32 tokens][128 m] output tile
 
     const uint32_t sbase = (smem_addr(smem_raw) + 1023u) & ~1023u;
     uint8_t* const sgen = smem_raw + (sbase - smem_addr(smem_raw));
     const uint32_t bar0 = smem_addr(&bars[0]);
-    auto FULL_W = [&](int s) { return bar0 + 8u * s; };
-    auto FULL_X = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
-    auto EMPTY = [&](int s) { return bar0 + 8u * (2 * kMaxStages + s); };
-    const uint32_t DONE = bar0 + 8u * (3 * kMaxStages);
+    auto FULL = [&](int s) { return bar0 + 8u * s; };
+    auto CONV = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto EMPTY = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
+    auto TFULL = [&](int a) { return bar0 + 8u * (3 * kStages + a); };
+    auto TEMPTY = [&](int a) { return bar0 + 8u * (3 * kStages + 2 + a); };
 
-    const uint32_t tmem_cols = NT <= 32 ? 32u : (NT <= 64 ? 64u : 128u);
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        for (int s = 0; s < kMaxStages; ++s) {
-            bar_init(FULL_W(s), 1);
-            bar_init(FULL_X(s), 128);
+        for (int s = 0; s < kStages; ++s) {
+            bar_init(FULL(s), 1);
+            bar_init(CONV(s), 128);
             bar_init(EMPTY(s), 1);
         }
-        bar_init(DONE, 1);
+        for (int a = 0; a < 2; ++a) {
+            bar_init(TFULL(a), 1);
+            bar_init(TEMPTY(a), 128);
+        }
         fence_barrier_init();
     }
     if (warp == 4) {
-        tmem_alloc(smem_addr(&tmem_slot), tmem_cols);
+        tmem_alloc(smem_addr(&tmem_slot), 2 * acc_cols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -120,130 +134,194 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_p = &abort_flag;
 
     if (warp == 4) {
-        // ---- weight producer ------------------------------------------------------------
+        // ---- TMA producer ---------------------------------------------------------------
         if (lane == 0) {
             tma_prefetch_desc(&w_map);
-            int last_issued[kMaxStages];
-            for (int s = 0; s < kMaxStages; ++s) last_issued[s] = -1;
-            for (int c = 0; c < nchunks; ++c) {
-                const int s = c % ST;
-                if (c >= ST && !wait_bar(EMPTY(s), ((c / ST) - 1) & 1, abort_p, nullptr)) break;
-                const uint32_t dst = sbase + s * stage_bytes;
-                bar_arrive_expect_tx(FULL_W(s), kWStage);
-                const int y = h * p.K + c * kKChunk;
-                tma_load_2d(dst, &w_map, FULL_W(s), m0, y);
-                tma_load_2d(dst + kWBox, &w_map, FULL_W(s), m0 + 64, y);
-                last_issued[s] = c;
+            tma_prefetch_desc(&x_map);
+            int g = 0;
+            int last[kStages] = {-1, -1, -1, -1};
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const Unit w = unit_of(u, n_tiles, m_tiles);
+                for (int c = 0; c < nchunks; ++c, ++g) {
+                    const int s = g % kStages;
+                    if (g >= kStages && !wait_bar(EMPTY(s), ((g / kStages) - 1) & 1, abort_p, nullptr)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = sbase + s * stage_bytes;
+                    bar_arrive_expect_tx(FULL(s), stage_bytes);
+                    const int wy = w.h * p.K + c * kKChunk;
+                    tma_load_2d(dst, &w_map, FULL(s), w.mt * 128, wy);
+                    tma_load_2d(dst + kWBox, &w_map, FULL(s), w.mt * 128 + 64, wy);
+                    if (p.x_f32) {
+                        tma_load_3d(dst + kWStage, &x_map, FULL(s), c * kKChunk, w.h, w.nt * NT);
+                        tma_load_3d(dst + kWStage + x_panel, &x_map, FULL(s), c * kKChunk + 32, w.h, w.nt * NT);
+                    } else {
+                        tma_load_3d(dst + kWStage, &x_map, FULL(s), c * kKChunk, w.h, w.nt * NT);
+                    }
+                    last[s] = g;
+                }
             }
-            // Wind-down after an abort: let the copies still in flight land before the CTA
-            // leaves (bounded as well).
-            if (*abort_p) {
-                int dummy = 0;
-                for (int s = 0; s < kMaxStages; ++s)
-                    if (last_issued[s] >= 0) wait_bar(FULL_W(s), (last_issued[s] / ST) & 1, &dummy, nullptr);
+            if (!ok) {  // let the copies still in flight land before the CTA leaves
+                int ignore = 0;
+                for (int s = 0; s < kStages; ++s)
+                    if (last[s] >= 0) wait_bar(FULL(s), (last[s] / kStages) & 1, &ignore, nullptr);
             }
         }
     } else if (warp == 5) {
         // ---- MMA issuer -----------------------------------------------------------------
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(128, NT, true, false);
+            int g = 0, i = 0;
             bool ok = true;
-            for (int c = 0; c < nchunks && ok; ++c) {
-                const int s = c % ST;
-                const uint32_t par = (c / ST) & 1;
-                ok = wait_bar(FULL_W(s), par, abort_p, nullptr) && wait_bar(FULL_X(s), par, abort_p, nullptr);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t wb = sbase + s * stage_bytes;
-                const uint32_t xb = wb + kWStage;
-#pragma unroll
-                for (int kk = 0; kk < kKChunk / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(wb + kk * 2048, kWBox, 1024);
-                    const uint64_t bd = smem_desc_sw128(xb + kk * 32, 16, 1024);
-                    mma_ss(tmem, ad, bd, idesc, (c | kk) != 0);
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
+                const int acc = i & 1;
+                if (i >= 2 && !wait_bar(TEMPTY(acc), ((i >> 1) - 1) & 1, abort_p, nullptr)) {
+                    ok = false;
+                    break;
                 }
-                if (p.x_f32) {
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)acc * acc_cols;
+                for (int c = 0; c < nchunks; ++c, ++g) {
+                    const int s = g % kStages;
+                    const uint32_t par = (g / kStages) & 1;
+                    if (!wait_bar(p.x_f32 ? CONV(s) : FULL(s), par, abort_p, nullptr)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t wb = sbase + s * stage_bytes;
+                    const uint32_t xb = wb + kWStage;
 #pragma unroll
                     for (int kk = 0; kk < kKChunk / 16; ++kk) {
                         const uint64_t ad = smem_desc_sw128(wb + kk * 2048, kWBox, 1024);
-                        const uint64_t bd = smem_desc_sw128(xb + x_panel + kk * 32, 16, 1024);
-                        mma_ss(tmem, ad, bd, idesc, 1u);
+                        mma_ss(d, ad, smem_desc_sw128(xb + kk * 32, 16, 1024), idesc, (c | kk) != 0);
+                        if (p.x_f32) mma_ss(d, ad, smem_desc_sw128(xb + x_panel + kk * 32, 16, 1024), idesc, 1u);
                     }
+                    mma_commit(EMPTY(s));
                 }
-                mma_commit(EMPTY(s));
+                if (ok) mma_commit(TFULL(acc));
             }
-            if (ok) mma_commit(DONE);
+        }
+    } else if (warp >= 6) {
+        if (!p.x_f32 && p.q_pe != nullptr) {
+            // ---- fused concat of the rope part (absorb): q[t, h, 512:576] = q_pe[t, h, :] --
+            const int tid = threadIdx.x - 192;
+            for (int u = blockIdx.x; u < units; u += gridDim.x) {
+                const Unit w = unit_of(u, n_tiles, m_tiles);
+                if (w.mt != 0) continue;
+                for (int it = tid; it < NT * 8; it += 128) {
+                    const int rr = it >> 3, c8 = it & 7;
+                    const int t = w.nt * NT + rr;
+                    if (t >= p.T) continue;
+                    const uint4 v = *reinterpret_cast<const uint4*>(p.q_pe + (int64_t)t * p.pe_st +
+                                                                    (int64_t)w.h * p.pe_sh + 8 * c8);
+                    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + (int64_t)t * p.out_st +
+                                              (int64_t)w.h * p.out_sh + kL + 8 * c8) = v;
+                }
+            }
+        }
+        // ---- fp32 activations -> bf16 hi / lo panels, in place --------------------------
+        if (p.x_f32) {
+            const int tid = threadIdx.x - 192;  // 0..127
+            const int per = NT / 16;            // (row, 8-value group) items per thread
+            int g = 0;
+            for (int u = blockIdx.x; u < units; u += gridDim.x) {
+                for (int c = 0; c < nchunks; ++c, ++g) {
+                    const int s = g % kStages;
+                    // After an abort the wait returns at once; the loop still runs every named
+                    // barrier so that no thread of the group is left waiting on another.
+                    wait_bar(FULL(s), (g / kStages) & 1, abort_p, nullptr);
+                    uint8_t* const xg = sgen + s * stage_bytes + kWStage;
+                    // staged layout: two unswizzled boxes [NT][32] fp32 (k 0-31, k 32-63)
+                    uint32_t hw[8][4], lw[8][4];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (j < per) {
+                            const int it = tid + 128 * j;
+                            const int r = it >> 3, c8 = it & 7;
+                            const float4* src =
+                                reinterpret_cast<const float4*>(xg + (c8 >> 2) * x_panel + r * 128 + (c8 & 3) * 32);
+                            const float4 a = src[0], b = src[1];
+                            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                hw[j][q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
+                                lw[j][q] = pack_bf16x2(v[2 * q] - bf16_lo_f(hw[j][q]),
+                                                       v[2 * q + 1] - bf16_hi_f(hw[j][q]));
+                            }
+                        }
+                    }
+                    named_bar(kBarConvert, 128);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (j < per) {
+                            const int it = tid + 128 * j;
+                            const int r = it >> 3, c8 = it & 7;
+                            const uint32_t so = (uint32_t)r * 128u + (uint32_t)((c8 ^ (r & 7)) * 16);
+                            *reinterpret_cast<uint4*>(xg + so) = make_uint4(hw[j][0], hw[j][1], hw[j][2], hw[j][3]);
+                            *reinterpret_cast<uint4*>(xg + x_panel + so) =
+                                make_uint4(lw[j][0], lw[j][1], lw[j][2], lw[j][3]);
+                        }
+                    }
+                    fence_proxy_async_cta();
+                    bar_arrive(CONV(s));
+                }
+            }
         }
     } else {
-        // ---- activation loaders (warps 0-3) ---------------------------------------------
-        const int tid = threadIdx.x;  // 0..127
-        const int items = NT * 8;     // (row, 16-byte chunk) pairs of one 64-deep panel
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c % ST;
-            if (c >= ST && !wait_bar(EMPTY(s), ((c / ST) - 1) & 1, abort_p, nullptr)) break;
-            uint8_t* const xg = sgen + s * stage_bytes + kWStage;
-            const int k0 = c * kKChunk;
-            for (int i = tid; i < items; i += 128) {
-                const int r = i >> 3, c16 = i & 7;
-                const int t = n0 + r;
-                uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
-                if (t < p.T) {
-                    const int64_t off = (int64_t)t * p.x_st + (int64_t)h * p.x_sh + k0 + 8 * c16;
-                    if (p.x_f32) {
-                        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + off);
-                        const float4 a = src[0], b = src[1];
-                        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                        uint32_t hw[4], lw[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            hw[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-                            lw[j] = pack_bf16x2(v[2 * j] - bf16_lo_f(hw[j]), v[2 * j + 1] - bf16_hi_f(hw[j]));
-                        }
-                        hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                    } else {
-                        hi = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + off);
-                    }
+        // ---- epilogue (warps 0-3): TMEM lane = m, column = token ------------------------
+        const int tid = threadIdx.x;
+        const uint32_t stage_base = sbase + kStages * stage_bytes;  // two slice tiles
+        uint8_t* const stage_gen = sgen + kStages * stage_bytes;
+        int i = 0, sc = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
+            const Unit w = unit_of(u, n_tiles, m_tiles);
+            const int acc = i & 1;
+            const bool ok = wait_bar(TFULL(acc), (i >> 1) & 1, abort_p, nullptr);
+            tc_fence_after();
+            for (int j0 = 0; j0 < NT; j0 += kSlice, ++sc) {
+                const int b = sc & 1;
+                if (sc >= 2) {  // the TMA store that last read tile b has finished reading it
+                    if (tid == 0) bulk_wait_group_read<1>();
+                    named_bar(kBarEpi, 128);
                 }
-                const uint32_t so = (uint32_t)r * 128u + (uint32_t)((c16 ^ (r & 7)) * 16);
-                *reinterpret_cast<uint4*>(xg + so) = hi;
-                if (p.x_f32) *reinterpret_cast<uint4*>(xg + x_panel + so) = lo;
-            }
-            fence_proxy_async_cta();
-            bar_arrive(FULL_X(s));
-        }
-        // Fused concat of the rope part (absorb only): q[t, h, 512:576] = q_pe[t, h, :].
-        if (p.q_pe != nullptr && blockIdx.x == 0) {
-            for (int i = tid; i < NT * 8; i += 128) {
-                const int r = i >> 3, c16 = i & 7;
-                const int t = n0 + r;
-                if (t >= p.T) continue;
-                const uint4 v = *reinterpret_cast<const uint4*>(p.q_pe + (int64_t)t * p.pe_st + (int64_t)h * p.pe_sh +
-                                                                8 * c16);
-                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + (int64_t)t * p.out_st +
-                                          (int64_t)h * p.out_sh + kL + 8 * c16) = v;
-            }
-        }
-        // ---- epilogue: TMEM lane = m, column = token ------------------------------------
-        const bool ok = wait_bar(DONE, 0, abort_p, nullptr);
-        tc_fence_after();
-        const int m = m0 + warp * 32 + lane;
-        for (int j0 = 0; j0 < NT; j0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)j0, r);
-            tmem_wait_ld();
+                uint32_t r[32];
+                if (ok) {
+                    tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)acc * acc_cols + (uint32_t)j0, r);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int t = n0 + j0 + jj;
-                if (j0 + jj < NT && t < p.T)
-                    store_out(p, t, m, ok ? __uint_as_float(r[jj]) : __int_as_float(0x7fc00000));
+                    for (int jj = 0; jj < 32; ++jj) r[jj] = 0x7fc00000u;  // NaN marks a CTA that gave up
+                }
+                uint8_t* const tile = stage_gen + b * slice_bytes;
+                if (p.out_f32) {
+                    float* const row = reinterpret_cast<float*>(tile) + tid;
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) row[jj * 128] = __uint_as_float(r[jj]);
+                } else {
+                    uint16_t* const row = reinterpret_cast<uint16_t*>(tile) + tid;
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj)
+                        row[jj * 128] = (uint16_t)(pack_bf16x2(__uint_as_float(r[jj]), 0.f) & 0xffffu);
+                }
+                fence_proxy_async_cta();
+                named_bar(kBarEpi, 128);
+                if (tid == 0) {
+                    tma_store_3d(&o_map, stage_base + b * slice_bytes, w.mt * 128, w.h, w.nt * NT + j0);
+                    bulk_commit_group();
+                }
             }
+            tc_fence_before();
+            bar_arrive(TEMPTY(acc));
         }
+        if (tid == 0) bulk_wait_group<0>();
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) tmem_dealloc(tmem, tmem_cols);
+    if (warp == 4) tmem_dealloc(tmem, 2 * acc_cols);
 }
 
 int pick_n_tile(int T) {
@@ -251,19 +329,51 @@ int pick_n_tile(int T) {
     return t16 < 128 ? t16 : 128;
 }
 
-cudaError_t launch_head_gemm(const HeadGemmArgs& a, const uint16_t* w, int M_total, cudaStream_t s) {
-    CUtensorMap map;
-    const uint64_t dims[2] = {(uint64_t)M_total, (uint64_t)a.H * a.K};
-    const uint64_t strides[1] = {(uint64_t)M_total * 2};
-    const uint32_t box[2] = {64, 64};
-    cudaError_t e = encode_tmap(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, dims, strides, box, true);
+// x: element (t, h, k) at x[t * x_st + h * x_sh + k], K values per (t, h) row.
+cudaError_t launch_head_gemm(HeadGemmArgs a, const uint16_t* w, const void* x, int64_t x_st, int64_t x_sh,
+                             cudaStream_t s) {
+    CUtensorMap wmap, xmap;
+    {
+        const uint64_t dims[2] = {(uint64_t)a.M_total, (uint64_t)a.H * a.K};
+        const uint64_t strides[1] = {(uint64_t)a.M_total * 2};
+        const uint32_t box[2] = {64, 64};
+        cudaError_t e = encode_tmap(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, dims, strides, box, true);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const uint64_t es = a.x_f32 ? 4 : 2;
+        // A stride of a dimension of extent 1 is never used; give it a harmless legal value.
+        if (a.H == 1) x_sh = a.K;
+        if (a.T == 1) x_st = x_sh * a.H;
+        const uint64_t dims[3] = {(uint64_t)a.K, (uint64_t)a.H, (uint64_t)a.T};
+        const uint64_t strides[2] = {(uint64_t)x_sh * es, (uint64_t)x_st * es};
+        const uint32_t box[3] = {a.x_f32 ? 32u : 64u, 1u, (uint32_t)a.n_tile};
+        cudaError_t e = encode_tmap(&xmap, a.x_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                    3, x, dims, strides, box, !a.x_f32);
+        if (e != cudaSuccess) return e;
+    }
+    CUtensorMap omap;
+    {
+        const uint64_t es = a.out_f32 ? 4 : 2;
+        const int64_t ost = a.T == 1 ? a.out_sh * a.H : a.out_st;
+        const uint64_t dims[3] = {(uint64_t)a.out_sh, (uint64_t)a.H, (uint64_t)a.T};
+        const uint64_t strides[2] = {(uint64_t)a.out_sh * es, (uint64_t)ost * es};
+        const uint32_t box[3] = {128u, 1u, (uint32_t)kSlice};
+        cudaError_t e = encode_tmap(&omap, a.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                    3, a.out, dims, strides, box, false);
+        if (e != cudaSuccess) return e;
+    }
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const int stage_bytes = kWStage + (a.x_f32 ? 2 : 1) * a.n_tile * 128;
-    const int smem = a.stages * stage_bytes + 1024;
+    const int smem = kStages * stage_bytes + 2 * kSlice * 128 * (a.out_f32 ? 4 : 2) + 1024;
     e = cudaFuncSetAttribute(head_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(M_total / 128, a.H, (a.T + a.n_tile - 1) / a.n_tile);
-    head_gemm_kernel<<<grid, kThreads, smem, s>>>(map, a);
+    const int units = ((a.T + a.n_tile - 1) / a.n_tile) * (a.M_total / 128) * a.H;
+    const int grid = units < sms ? units : sms;
+    head_gemm_kernel<<<grid, kThreads, smem, s>>>(wmap, xmap, omap, a);
     return cudaGetLastError();
 }
 
@@ -276,12 +386,9 @@ cudaError_t launch_absorb_sm103(const uint16_t* q_nope, int64_t snt, int64_t snh
     a.T = T;
     a.H = H;
     a.K = kP;
+    a.M_total = kL;
     a.n_tile = pick_n_tile(T);
-    a.stages = 2;
-    a.x = q_nope;
     a.x_f32 = 0;
-    a.x_st = snt;
-    a.x_sh = snh;
     a.out = q_out;
     a.out_f32 = 0;
     a.out_st = (int64_t)H * kD;
@@ -289,7 +396,7 @@ cudaError_t launch_absorb_sm103(const uint16_t* q_nope, int64_t snt, int64_t snh
     a.q_pe = q_pe;
     a.pe_st = spt;
     a.pe_sh = sph;
-    return launch_head_gemm(a, w_uk_t, kL, s);
+    return launch_head_gemm(a, w_uk_t, q_nope, snt, snh, s);
 }
 
 cudaError_t launch_out_proj_sm103(const void* o_latent, int in_dtype, const uint16_t* w_uv, void* o,
@@ -298,18 +405,15 @@ cudaError_t launch_out_proj_sm103(const void* o_latent, int in_dtype, const uint
     a.T = T;
     a.H = H;
     a.K = kL;
+    a.M_total = kV;
     a.n_tile = pick_n_tile(T);
-    a.stages = kMaxStages;
-    a.x = o_latent;
     a.x_f32 = in_dtype == MLA_DT_F32;
-    a.x_st = (int64_t)H * kL;
-    a.x_sh = kL;
     a.out = o;
     a.out_f32 = out_dtype == MLA_DT_F32;
     a.out_st = (int64_t)H * kV;
     a.out_sh = kV;
     a.q_pe = nullptr;
-    return launch_head_gemm(a, w_uv, kV, s);
+    return launch_head_gemm(a, w_uv, o_latent, (int64_t)H * kL, kL, s);
 }
 
 }  // namespace mla

@@ -141,6 +141,8 @@ mla_status mla_absorb_q(const void* q_nope, int64_t snt, int64_t snh, const void
         return fail(MLA_ERR_UNSUPPORTED, "mla_absorb_q: strides must be non-negative multiples of 8");
     if (snh < mla::kP && H > 1)
         return fail(MLA_ERR_INVALID_ARG, "mla_absorb_q: q_nope head stride %lld < 128", (long long)snh);
+    if (snt == 0 && T > 1)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_absorb_q: q_nope token stride 0 (broadcast) is not supported");
     cudaError_t e = mla::launch_absorb_sm103((const uint16_t*)q_nope, snt, snh, (const uint16_t*)q_pe, spt,
                                            sph, (const uint16_t*)W_UK_T, (uint16_t*)q_out, T, H,
                                            (cudaStream_t)stream);

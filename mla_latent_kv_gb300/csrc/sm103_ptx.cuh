@@ -162,6 +162,29 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const void* map, int32_t x, i
                  : "memory");
 }
 
+// TMA store of one box from this CTA's shared memory to global memory (elements outside the
+// tensor are not written), tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int32_t x, int32_t y, int32_t z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's bulk async-groups still read their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until at most N of this thread's bulk async-groups are incomplete.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to another CTA's shared
 // memory of the cluster; completion is counted (complete_tx) on the barrier `remote_bar`, which
 // lives in the destination CTA. Both addresses are shared::cluster addresses (see map_to_rank).
