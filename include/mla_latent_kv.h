@@ -104,6 +104,17 @@ int mla_resolve_num_splits(int num_splits, int B, int Sq, int H, int max_seq_len
  * because the LSE precision decides the merge). Host only. */
 size_t mla_decode_workspace_bytes(int B, int Sq, int H, int num_splits);
 
+/* Bytes of workspace mla_decode needs for a cache of format kv_dtype (valid for both formats;
+ * for MLA_KV_BF16 it equals mla_decode_workspace_bytes). For the FP8 format it adds, after the
+ * split-KV partials (each region 256-byte aligned), the first stage's expanded pages:
+ * B * ceil(max_seq_len / 64) * 64 rows of 576 bf16 plus two fp32 scales per row. The 584-byte
+ * FP8 row is not a multiple of 16 bytes, so TMA cannot tile it; mla_decode re-lays the pages a
+ * batch reads out as exact bf16 values (e4m3 -> bf16 is lossless) and applies k_scale / v_scale
+ * in fp32 inside the attention kernel. 0 for an unknown kv_dtype or a non-positive shape. Host
+ * only. */
+size_t mla_decode_workspace_bytes_kv(mla_kv_dtype kv_dtype, int B, int Sq, int H, int num_splits,
+                                     int max_seq_len);
+
 /*
  * Query absorption ([vLLM-MLA, two-algorithms section]: ql_nope = q_nope W_UK^T, concatenated
  * with q_pe; [TRT-TP, absorption section]: fused_q = [q_nope W_kb^T || q_pe]):
@@ -145,12 +156,15 @@ mla_status mla_absorb_q(const void* q_nope, int64_t q_nope_stride_t, int64_t q_n
  *               MLA_DEV_SEQ_TOO_LONG and the row's output is undefined)
  *   num_splits  split-KV request, see mla_resolve_num_splits (1 = no split, deterministic
  *               per-row reduction order independent of the batch, [vLLM-MLA, FlashMLA section])
- *   workspace   device scratch of >= mla_decode_workspace_bytes(B, Sq, H, resolved splits)
- *               bytes (may be NULL when that is 0); contents on entry are ignored
+ *   workspace   device scratch of >= mla_decode_workspace_bytes_kv(kv_dtype, B, Sq, H,
+ *               resolved splits, max_seq_len) bytes, 256-byte aligned (may be NULL when that is
+ *               0); contents on entry are ignored
  *   o_latent    [B, Sq, H, 512] of o_dtype (fp32 recommended; bf16 rounds the result once)
  *   lse         fp32 [B, Sq, H], may be NULL
  *   dev_status  int32 device word or NULL; MLA_DEV_* bits are OR-ed into it, never cleared
- * Limits: 1 <= H <= 128, Sq >= 1, B >= 0 (B == 0 launches nothing), page size 64.
+ * Limits: 1 <= H <= 128, Sq >= 1, B >= 0 (B == 0 launches nothing), page size 64; FP8 cache:
+ * ceil(max_seq_len / 64) <= 65535. FP8 precision: k_scale multiplies the fp32 score and v_scale
+ * the fp32 softmax weight before its one rounding to bf16 for the PV product.
  */
 mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype, int64_t num_blocks,
                       const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
@@ -175,14 +189,16 @@ mla_status mla_out_proj(const void* o_latent, mla_dtype in_dtype, const void* W_
  * they decode: serving loops that run under a fixed device-memory budget with every buffer made
  * at start-up, host runtimes that forbid device allocations after initialisation, and call paths
  * that cannot carry a workspace pointer down to the attention call. (The pages have no
- * counterpart of this call; it only changes where the split-KV scratch lives.)
+ * counterpart of this call; it only changes where the decode scratch lives.)
  *
  * Same arguments, meaning and results as mla_decode, minus workspace / workspace_bytes. The
  * split-KV partials live in one file-scope device array of mla_decode_noalloc_max_workspace_bytes()
- * bytes (64 MiB), held on every device that uses it until the process exits. The first call on a
+ * bytes (64 MiB), held on every device that uses it until the process exits; a call whose
+ * mla_decode_workspace_bytes_kv exceeds that (most FP8-cache batches: the expanded pages live
+ * in the same scratch) is refused with MLA_ERR_WORKSPACE_TOO_SMALL. The first call on a
  * device looks up the array's device address (once per device, with that device current); make
- * that first call before any stream capture. Split plans that need more than the array holds are
- * refused with MLA_ERR_WORKSPACE_TOO_SMALL before any launch. Nothing here calls cudaMalloc,
+ * that first call before any stream capture. The size check comes before any launch. Nothing
+ * here calls cudaMalloc,
  * cudaFree or any allocating library routine. All calls share the array: calls whose kernels
  * overlap on the GPU (e.g. issued on different streams) race on it and must be serialised by
  * the caller. The array keeps the last call's contents; no result depends on them.

@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         l.mla_resolve_num_splits.argtypes = [i32, i32, i32, i32, i32]
         l.mla_decode_workspace_bytes.restype = sz
         l.mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        l.mla_decode_workspace_bytes_kv.restype = sz
+        l.mla_decode_workspace_bytes_kv.argtypes = [i32, i32, i32, i32, i32, i32]
         l.mla_absorb_q.restype = i32
         l.mla_absorb_q.argtypes = [vp, i64, i64, vp, i64, i64, vp, vp, i32, i32, vp]
         l.mla_decode.restype = i32
@@ -102,8 +104,11 @@ def resolve_num_splits(num_splits: int, B: int, Sq: int, H: int, max_seq_len: in
     return s
 
 
-def workspace_bytes(B: int, Sq: int, H: int, num_splits: int) -> int:
-    return int(lib().mla_decode_workspace_bytes(B, Sq, H, num_splits))
+def workspace_bytes(B: int, Sq: int, H: int, num_splits: int, kv_dtype: int = KV_BF16, max_seq_len: int = 0) -> int:
+    """Decode workspace bytes; with the default kv_dtype this is the split-KV part alone."""
+    if kv_dtype == KV_BF16:
+        return int(lib().mla_decode_workspace_bytes(B, Sq, H, num_splits))
+    return int(lib().mla_decode_workspace_bytes_kv(kv_dtype, B, Sq, H, num_splits, max_seq_len))
 
 
 # ----------------------------------------------------------------------------- torch front end
@@ -143,7 +148,7 @@ def decode(q, kv_cache, block_table, seq_lens, max_seq_len, scale, kv_dtype=KV_B
     if num_blocks is None:
         num_blocks = kv_cache.numel() * kv_cache.element_size() // (PAGE * row_bytes(kv_dtype))
     S = resolve_num_splits(num_splits, B, Sq, H, max_seq_len)
-    need = workspace_bytes(B, Sq, H, S)
+    need = workspace_bytes(B, Sq, H, S, kv_dtype, max_seq_len)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     if o_latent is None:

@@ -57,6 +57,10 @@ using namespace ptx;
 
 constexpr int kThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (CTA 0) / 2-5 helpers (CTA 1)
 constexpr int kPPG = 4;              // pages per group
+#ifndef MLA_PREFETCH_GROUPS
+#define MLA_PREFETCH_GROUPS 1
+#endif
+constexpr int kPrefetchGroups = MLA_PREFETCH_GROUPS;  // L2 prefetch distance in groups
 constexpr int kSlots = 4;            // CTA 0 K ring slots
 constexpr int kPageBox = 64 * 128;   // one page's rows of one 64-dim panel (8 KB)
 constexpr int kSlotBytes = kPPG * kPageBox;  // 32 KB
@@ -125,7 +129,8 @@ __device__ __forceinline__ RowGeom row_geometry(const DecodeArgs& p, int unit, b
     g.b = g.r / p.Sq;
     g.t = g.r % p.Sq;
     int seq = p.seq_lens[g.b];
-    const int cap = p.max_blocks * kPage;
+    // FP8 cache: the expanded layout holds fp8_mp pages per request
+    const int cap = (p.fp8_mp > 0 && p.fp8_mp < p.max_blocks ? p.fp8_mp : p.max_blocks) * kPage;
     if (seq > cap || seq > p.max_seq_len || seq < 0) {
         if (report && p.dev_status) atomicOr(p.dev_status, MLA_DEV_SEQ_TOO_LONG);
         seq = seq < 0 ? 0 : (seq > cap ? cap : seq);
@@ -139,8 +144,11 @@ __device__ __forceinline__ RowGeom row_geometry(const DecodeArgs& p, int unit, b
 }
 
 // Physical first row of page `pg` of request b, or one past the cache (the TMA then fills
-// zeros) if the block-table entry is out of range.
+// zeros) if the block-table entry is out of range. FP8 cache: the row in the expanded layout
+// (the first stage already resolved the block table and reported bad entries).
+template <bool kFp8>
 __device__ __forceinline__ int page_row(const DecodeArgs& p, int b, int pg) {
+    if constexpr (kFp8) return (b * p.fp8_mp + pg) * kPage;
     int32_t blk = p.block_table[(size_t)b * p.max_blocks + pg];
     if (blk < 0 || (int64_t)blk >= p.num_blocks) {
         if (p.dev_status) atomicOr(p.dev_status, MLA_DEV_BAD_BLOCK_ID);
@@ -159,6 +167,7 @@ __device__ __forceinline__ int valid_rows(const RowGeom& g, int page) {
     return page < g.npages ? min(kPage, g.j1 - (g.j0 + kPage * page)) : 0;
 }
 
+template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_sm103_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                         const DecodeArgs p) {
@@ -212,10 +221,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tma_load_2d(sbase + OFF_QROPE, &q_map, bar(B_QFULL), 8 * 64, g.r * p.H);
                 int issued = 0;  // K panels issued
                 bool ok = true;
+                // L2 prefetch of whole pages kPrefetchGroups groups ahead of the ring, so that the
+                // ring's loads see L2 rather than DRAM latency.
+                const uint8_t* kv_rows = kFp8 ? reinterpret_cast<const uint8_t*>(p.fp8_rows) : p.cache;
+                const int pf_end = min(npages, kPPG * kPrefetchGroups);
+                for (int pg = 0; pg < pf_end; ++pg) {
+                    const int yr = page_row<kFp8>(p, g.b, g.page0 + pg);
+                    if (kFp8 || yr < p.num_blocks * kPage)
+                        bulk_prefetch_l2(kv_rows + (size_t)yr * kBf16RowBytes, kPage * kBf16RowBytes);
+                }
                 for (int gi = 0; gi < ngroups && ok; ++gi) {
                     int y[kPPG];
                     const int np = min(kPPG, npages - kPPG * gi);
-                    for (int q = 0; q < np; ++q) y[q] = page_row(p, g.b, g.page0 + kPPG * gi + q);
+                    for (int q = 0; q < np; ++q) y[q] = page_row<kFp8>(p, g.b, g.page0 + kPPG * gi + q);
+                    for (int q = 0; q < kPPG; ++q) {
+                        const int pg = kPPG * (gi + kPrefetchGroups) + q;
+                        if (pg >= npages) break;
+                        const int yr = page_row<kFp8>(p, g.b, g.page0 + pg);
+                        if (kFp8 || yr < p.num_blocks * kPage)
+                            bulk_prefetch_l2(kv_rows + (size_t)yr * kBf16RowBytes, kPage * kBf16RowBytes);
+                    }
                     for (int pn = 0; pn < 9; ++pn) {
                         const int m = 9 * gi + pn, slot = m % kSlots, k = m / kSlots;
                         ok = k == 0 ? wait_bar(bar(B_QREADY), 0, abort, ds)  // Q's panels moved out
@@ -339,12 +364,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 const int pg0 = kPPG * gi + 2 * half;  // first of this half's two pages
                 const int valid0 = valid_rows(g, pg0), valid1 = valid_rows(g, pg0 + 1);
+                // FP8 cache: lane i holds (k_scale, v_scale) of token i of each 32-token chunk;
+                // tokens past the last visible one keep 0 so that no stale scale reaches P.
+                float ksc[4] = {0.f, 0.f, 0.f, 0.f}, vsc[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (kFp8) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int v = c < 2 ? valid0 - 32 * c : valid1 - 32 * (c - 2);
+                        if (lane < v) {
+                            const size_t tok = ((size_t)g.b * p.fp8_mp + g.page0 + pg0 + (c >> 1)) * kPage +
+                                               32 * (c & 1) + lane;
+                            const float2 sc = reinterpret_cast<const float2*>(p.fp8_scales)[tok];
+                            ksc[c] = sc.x;
+                            vsc[c] = sc.y;
+                        }
+                    }
+                }
                 float lm = -CUDART_INF_F;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int v = c < 2 ? valid0 - 32 * c : valid1 - 32 * (c - 2);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
+                        if constexpr (kFp8) {  // K = e4m3 * k_scale: the scale multiplies the score
+                            const float ks = __shfl_sync(0xffffffffu, ksc[c], j);
+                            s[c][j] = __float_as_uint(__uint_as_float(s[c][j]) * ks);
+                        }
                         if (j >= v) s[c][j] = __float_as_uint(-CUDART_INF_F);
                         lm = fmaxf(lm, __uint_as_float(s[c][j]));
                     }
@@ -370,10 +415,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const float a1 = fast_exp2(fmaf(__uint_as_float(s[2 * q][2 * c + 1]), sl2, -m_run));
                         const float b0 = fast_exp2(fmaf(__uint_as_float(s[2 * q + 1][2 * c]), sl2, -m_run));
                         const float b1 = fast_exp2(fmaf(__uint_as_float(s[2 * q + 1][2 * c + 1]), sl2, -m_run));
-                        pk[c] = pack_bf16x2(a0, a1);
-                        pk[16 + c] = pack_bf16x2(b0, b1);
-                        lt_run += (a0 + a1) + (b0 + b1);
-                        l_run += (bf16_lo_f(pk[c]) + bf16_hi_f(pk[c])) + (bf16_lo_f(pk[16 + c]) + bf16_hi_f(pk[16 + c]));
+                        if constexpr (kFp8) {
+                            // V = e4m3 * v_scale: the scale multiplies the weight before its one
+                            // rounding; O is normalised by the unscaled sum.
+                            pk[c] = pack_bf16x2(a0 * __shfl_sync(0xffffffffu, vsc[2 * q], 2 * c),
+                                                a1 * __shfl_sync(0xffffffffu, vsc[2 * q], 2 * c + 1));
+                            pk[16 + c] = pack_bf16x2(b0 * __shfl_sync(0xffffffffu, vsc[2 * q + 1], 2 * c),
+                                                     b1 * __shfl_sync(0xffffffffu, vsc[2 * q + 1], 2 * c + 1));
+                            lt_run += (a0 + a1) + (b0 + b1);
+                            l_run += (a0 + a1) + (b0 + b1);
+                        } else {
+                            pk[c] = pack_bf16x2(a0, a1);
+                            pk[16 + c] = pack_bf16x2(b0, b1);
+                            lt_run += (a0 + a1) + (b0 + b1);
+                            l_run += (bf16_lo_f(pk[c]) + bf16_hi_f(pk[c])) +
+                                     (bf16_lo_f(pk[16 + c]) + bf16_hi_f(pk[16 + c]));
+                        }
                     }
                     if (page < npages && okS) {
                         const int stg = page % kPBufs, ust = page / kPBufs;
@@ -441,7 +498,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (kv > 0 && !wait_bar(bar(B_VEMPTY + st), (kv - 1) & 1, abort, ds)) break;
                     const uint32_t full = bar(B_VFULL + st);
                     bar_arrive_expect_tx(full, kVStageBytes);
-                    const int y = page_row(p, g.b, g.page0 + i);
+                    const int y = page_row<kFp8>(p, g.b, g.page0 + i);
                     const uint32_t dst = sbase + OFF_V + st * kVStageBytes;
 #pragma unroll
                     for (int pn = 0; pn < 8; ++pn) tma_load_2d(dst + pn * kPageBox, &kv_map, full, pn * 64, y);
@@ -599,27 +656,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();
 }
 
-int g_attr_done[64] = {0};
+int g_attr_done[2][64] = {};
 
 }  // namespace
 
 cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s) {
+    const bool fp8 = a.fp8_mp > 0;
+    auto* kernel = fp8 ? decode_sm103_kernel<true> : decode_sm103_kernel<false>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !g_attr_done[dev]) {
-        e = cudaFuncSetAttribute(decode_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (dev < 64 && !g_attr_done[fp8][dev]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        g_attr_done[dev] = 1;
+        g_attr_done[fp8][dev] = 1;
     }
     CUtensorMap kv_map, q_map;
     memset(&kv_map, 0, sizeof kv_map);
     memset(&q_map, 0, sizeof q_map);
     if (a.num_blocks > 0 && a.max_seq_len > 0) {
-        const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)a.num_blocks * kPage};
+        // bf16 rows of the cache itself, or of the FP8 cache's expanded pages
+        const uint64_t rows = fp8 ? (uint64_t)a.B * a.fp8_mp * kPage : (uint64_t)a.num_blocks * kPage;
+        const uint64_t dims[2] = {(uint64_t)kD, rows};
         const uint64_t strides[1] = {(uint64_t)kBf16RowBytes};
         const uint32_t box[2] = {64, 64};
-        e = encode_tmap(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.cache, dims, strides, box, true);
+        e = encode_tmap(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, fp8 ? (const void*)a.fp8_rows : a.cache, dims,
+                        strides, box, true);
         if (e != cudaSuccess) return e;
         const uint64_t qdims[2] = {(uint64_t)kD, (uint64_t)a.B * a.Sq * a.H};
         const uint32_t qbox[2] = {64, 128};
@@ -627,7 +689,7 @@ cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     const int64_t units = (int64_t)a.B * a.Sq * a.num_splits;
-    decode_sm103_kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, s>>>(kv_map, q_map, a);
+    kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, s>>>(kv_map, q_map, a);
     return cudaGetLastError();
 }
 

@@ -36,7 +36,18 @@ struct DecodeArgs {
     int o_dtype;                // mla_dtype
     float* lse;                 // [B, Sq, H] or null
     int32_t* dev_status;        // or null
+    // FP8 cache only: pages expanded by the first stage into bf16 rows + per-token scales
+    uint16_t* fp8_rows;         // [B * fp8_mp * 64, 576] bf16 (exact e4m3 values)
+    float* fp8_scales;          // [B * fp8_mp * 64, 2] (k_scale, v_scale)
+    int fp8_mp;                 // pages per request in that layout: ceil(max_seq_len / 64)
 };
+
+// Workspace carve-up of a decode call: split-KV partials first, then (FP8 cache) the expanded
+// rows and their scales; every region starts on a 256-byte boundary.
+struct WorkspaceLayout {
+    size_t part_o, part_lse, fp8_rows, fp8_scales, total;
+};
+WorkspaceLayout workspace_layout(int kv_dtype, int B, int Sq, int H, int num_splits, int max_seq_len);
 
 // Token range [j0, j1) of split s of a row with n visible tokens: the row is cut into
 // num_splits page-aligned chunks of round_up(ceil(n / S), 64) tokens; trailing splits may be
@@ -55,6 +66,7 @@ mla_status set_error(mla_status st, const char* fmt, ...);
 
 cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_fp8_expand(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_absorb_sm103(const uint16_t* q_nope, int64_t snt, int64_t snh, const uint16_t* q_pe,
                                 int64_t spt, int64_t sph, const uint16_t* w_uk_t, uint16_t* q_out, int T, int H,
                                 cudaStream_t s);

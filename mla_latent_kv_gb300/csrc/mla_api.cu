@@ -48,6 +48,28 @@ int device_sm_count() {
 }  // namespace
 
 namespace mla {
+WorkspaceLayout workspace_layout(int kv_dtype, int B, int Sq, int H, int num_splits, int max_seq_len) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    WorkspaceLayout w{};
+    if (B <= 0 || Sq <= 0 || H <= 0) return w;
+    size_t off = 0;
+    if (num_splits > 1) {
+        const size_t units = (size_t)B * Sq * num_splits * H;
+        w.part_o = 0;
+        w.part_lse = up(units * kL * sizeof(float));
+        off = w.part_lse + up(units * sizeof(float));
+    }
+    if (kv_dtype == MLA_KV_FP8_E4M3_SCALED && max_seq_len > 0) {
+        const size_t rows = (size_t)B * ((max_seq_len + kPage - 1) / kPage) * kPage;
+        w.fp8_rows = off;
+        off += up(rows * kBf16RowBytes);
+        w.fp8_scales = off;
+        off += up(rows * 2 * sizeof(float));
+    }
+    w.total = off;
+    return w;
+}
+
 mla_status set_error(mla_status st, const char* fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -120,12 +142,12 @@ int mla_resolve_num_splits(int num_splits, int B, int Sq, int H, int max_seq_len
 }
 
 size_t mla_decode_workspace_bytes(int B, int Sq, int H, int num_splits) {
-    if (B <= 0 || Sq <= 0 || H <= 0 || num_splits <= 1) return 0;
-    size_t units = (size_t)B * Sq * num_splits * H;
-    size_t o_bytes = units * mla::kL * sizeof(float);
-    size_t lse_bytes = units * sizeof(float);
-    size_t total = ((o_bytes + 255) / 256) * 256 + ((lse_bytes + 255) / 256) * 256;
-    return total;
+    return mla::workspace_layout(MLA_KV_BF16, B, Sq, H, num_splits, 0).total;
+}
+
+size_t mla_decode_workspace_bytes_kv(mla_kv_dtype kv_dtype, int B, int Sq, int H, int num_splits, int max_seq_len) {
+    if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3_SCALED) return 0;
+    return mla::workspace_layout(kv_dtype, B, Sq, H, num_splits, max_seq_len).total;
 }
 
 mla_status mla_absorb_q(const void* q_nope, int64_t snt, int64_t snh, const void* q_pe, int64_t spt,
@@ -176,8 +198,8 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
         return fail(MLA_ERR_INVALID_ARG, "mla_decode: null pointer");
     if (!aligned16(q) || (kv_cache && !aligned16(kv_cache)) || !aligned16(o_latent))
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: q, kv_cache and o_latent must be 16-byte aligned");
-    if (kv_dtype == MLA_KV_FP8_E4M3_SCALED)
-        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: FP8 cache not available in this build");
+    if (kv_dtype == MLA_KV_FP8_E4M3_SCALED && (max_seq_len + mla::kPage - 1) / mla::kPage > 65535)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: FP8 cache with max_seq_len=%d above 65535 pages", max_seq_len);
     if (num_blocks > (int64_t)(INT32_MAX / mla::kPage))
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: num_blocks=%lld too large (max %d)", (long long)num_blocks,
                     INT32_MAX / mla::kPage);
@@ -187,10 +209,13 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: B*Sq*H=%lld too large", (long long)B * Sq * H);
     if ((int64_t)B * Sq * S > (int64_t)1 << 30)
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: B*Sq*num_splits=%lld too large", (long long)B * Sq * S);
-    size_t need = mla_decode_workspace_bytes(B, Sq, H, S);
+    const mla::WorkspaceLayout wl = mla::workspace_layout(kv_dtype, B, Sq, H, S, max_seq_len);
+    const size_t need = wl.total;
     if (need > 0 && (workspace == nullptr || workspace_bytes < need))
-        return fail(MLA_ERR_WORKSPACE_TOO_SMALL, "mla_decode: workspace %zu bytes < %zu needed for %d splits",
-                    workspace ? workspace_bytes : (size_t)0, need, S);
+        return fail(MLA_ERR_WORKSPACE_TOO_SMALL,
+                    "mla_decode: workspace %zu bytes < %zu needed (%d splits%s)",
+                    workspace ? workspace_bytes : (size_t)0, need, S,
+                    kv_dtype == MLA_KV_FP8_E4M3_SCALED ? ", FP8 pages expanded" : "");
     if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: workspace must be 256-byte aligned");
 
@@ -209,17 +234,26 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
     a.scale = scale;
     a.num_splits = S;
     if (S > 1) {
-        size_t units = (size_t)B * Sq * S * H;
-        size_t o_bytes = ((units * mla::kL * sizeof(float) + 255) / 256) * 256;
-        a.part_o = (float*)workspace;
-        a.part_lse = (float*)((char*)workspace + o_bytes);
+        a.part_o = (float*)((char*)workspace + wl.part_o);
+        a.part_lse = (float*)((char*)workspace + wl.part_lse);
+    }
+    const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3_SCALED && max_seq_len > 0;
+    if (fp8) {
+        a.fp8_rows = (uint16_t*)((char*)workspace + wl.fp8_rows);
+        a.fp8_scales = (float*)((char*)workspace + wl.fp8_scales);
+        a.fp8_mp = (max_seq_len + mla::kPage - 1) / mla::kPage;
     }
     a.o_latent = o_latent;
     a.o_dtype = o_dtype;
     a.lse = lse;
     a.dev_status = dev_status;
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = mla::launch_decode_sm103(a, st);
+    cudaError_t e = cudaSuccess;
+    if (fp8) {
+        e = mla::launch_fp8_expand(a, st);
+        if (e != cudaSuccess) return cuda_fail(e, "mla_decode FP8 expand launch");
+    }
+    e = mla::launch_decode_sm103(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
     if (S > 1) {
         e = mla::launch_merge(a, st);

@@ -63,10 +63,10 @@ extern "C" mla_status mla_decode_noalloc(const void* q, const void* kv_cache, ml
     if (B > 0 && Sq > 0 && H >= 1 && H <= MLA_MAX_HEADS && num_splits >= -1 && max_seq_len >= 0) {
         const int S = mla_resolve_num_splits(num_splits, B, Sq, H, max_seq_len);
         if (S >= 1) {
-            const size_t need = mla_decode_workspace_bytes(B, Sq, H, S);
+            const size_t need = mla_decode_workspace_bytes_kv(kv_dtype, B, Sq, H, S, max_seq_len);
             if (need > kNoAllocScratchBytes)
                 return mla::set_error(MLA_ERR_WORKSPACE_TOO_SMALL,
-                                      "mla_decode_noalloc: %d splits x B*Sq=%lld x H=%d need %zu bytes of split "
+                                      "mla_decode_noalloc: %d splits x B*Sq=%lld x H=%d need %zu bytes of "
                                       "scratch, more than its fixed %zu bytes; use fewer splits or mla_decode",
                                       S, (long long)B * Sq, H, need, kNoAllocScratchBytes);
         }

@@ -155,6 +155,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
         : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16) of contiguous global memory into L2 (no shared memory,
+// no completion tracking).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gptr)), "r"(bytes)
+                 : "memory");
+}
+
 // Prefetch one box of a tensor into L2 (no shared memory, no completion tracking).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* map, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),

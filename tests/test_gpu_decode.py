@@ -86,6 +86,46 @@ def test_batch_zero_and_workspace_checks():
     assert e.value.status == mla.ERR_WORKSPACE_TOO_SMALL
 
 
+# ----------------------------------------------------------------------------- FP8 cache
+def _fp8_case(B, Sq, H, lens, seed, vscale=2.0):
+    """FP8 cache with v_scale = vscale * k_scale, so that swapping the two scales cannot pass."""
+    c = mi.decode_case(B, Sq, H, lens, kv=mi.KV_FP8, seed=seed)
+    cache = c["cache"].reshape(c["num_blocks"], 64, 584)
+    ks = cache[:, :, 576:580].copy().view("<f4")
+    vs = (ks * np.float32(vscale)).astype("<f4")
+    with np.errstate(invalid="ignore"):
+        cache[:, :, 580:584] = vs.view(np.uint8).reshape(cache.shape[0], 64, 4)
+    return dict(c, cache=cache.reshape(c["num_blocks"], -1))
+
+
+@pytest.mark.parametrize("num_splits", [1, 3, -1])
+def test_fp8_ragged_multi_page(num_splits):
+    c = _fp8_case(5, 1, 128, [1, 63, 65, 700, 1000], seed=26)
+    o, lse, st = run_decode(c, num_splits)
+    o_ref, lse_ref = _oracle(c)
+    assert st == 0
+    err = compare_decode(o, lse, o_ref, lse_ref, fp8=True)
+    print("fp8 errors", err)
+    # the only rounding beyond fp32 is P * v_scale -> bf16: far inside the FP8 bound
+    assert err["rel_l2"] <= 5e-3 and err["lse_max"] <= 1e-3, err
+
+
+def test_fp8_causal_two_rows_and_heads():
+    c = _fp8_case(3, 2, 20, [0, 2, 333], seed=27, vscale=0.5)
+    o, lse, st = run_decode(c, 2)
+    o_ref, lse_ref = _oracle(c)
+    assert st == 0
+    compare_decode(o, lse, o_ref, lse_ref, fp8=True)
+
+
+def test_fp8_bad_block_id_sets_device_status():
+    c = _fp8_case(2, 1, 16, [100, 100], seed=28)
+    bt = c["block_table"].copy()
+    bt[0, 1] = -3
+    _, _, st = run_decode(dict(c, block_table=bt), 1)
+    assert st & 0x1
+
+
 # ----------------------------------------------------------------------------- full workloads
 def _sampled(c, heads=(0, 37, 127)):
     sel = [(b, t, h) for b in range(c["B"]) for t in range(c["Sq"]) for h in heads if h < c["H"]]
@@ -94,7 +134,7 @@ def _sampled(c, heads=(0, 37, 127)):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name,num_splits", [("dsv3", -1), ("dsv3", 0), ("ragged", -1), ("long_mtp", 0),
-                                             ("long_mtp", -1)])
+                                             ("long_mtp", -1), ("fp8", -1), ("fp8", 0)])
 def test_full_workload_sampled(name, num_splits):
     c = mi.workload_case(name)
     o, lse, st = run_decode(c, num_splits)
@@ -102,7 +142,7 @@ def test_full_workload_sampled(name, num_splits):
     sel = _sampled(c)
     o_ref, lse_ref = _oracle(c, sel)
     idx = (sel[:, 0] * c["Sq"] + sel[:, 1]) * c["H"] + sel[:, 2]
-    compare_decode(o.reshape(-1, 512)[idx], lse.reshape(-1)[idx], o_ref, lse_ref)
+    compare_decode(o.reshape(-1, 512)[idx], lse.reshape(-1)[idx], o_ref, lse_ref, fp8=c["kv"] == mi.KV_FP8)
     # every row of the full output: finite, lse finite exactly where the row has tokens
     n = np.array([[oracle.row_len(int(s), c["Sq"], t) for t in range(c["Sq"])] for s in c["seq_lens"]])
     assert np.isfinite(o).all()

@@ -101,3 +101,16 @@ def test_workload_table_matches_configs():
     import numpy as np
     lens = mi.draw_lengths("loguniform", 128, np.random.default_rng(2))
     assert list(lens[:6]) == [1, 63, 64, 65, 128, 32768] and lens.min() >= 1 and lens.max() <= 32768
+
+
+def test_workspace_bytes_by_cache_format(lib):
+    up = lambda x: (x + 255) // 256 * 256
+    B, Sq, H, S, L = 3, 2, 16, 4, 130
+    split = up(B * Sq * S * H * 512 * 4) + up(B * Sq * S * H * 4)
+    assert mla.workspace_bytes(B, Sq, H, S) == split
+    assert mla.workspace_bytes(B, Sq, H, S, mla.KV_BF16, L) == split
+    rows = B * 3 * 64  # ceil(130 / 64) = 3 pages per request
+    fp8 = split + up(rows * 1152) + up(rows * 8)
+    assert mla.workspace_bytes(B, Sq, H, S, mla.KV_FP8, L) == fp8
+    assert mla.workspace_bytes(B, Sq, H, 1, mla.KV_FP8, L) == up(rows * 1152) + up(rows * 8)
+    assert lib.mla_decode_workspace_bytes_kv(7, B, Sq, H, S, L) == 0
