@@ -239,7 +239,7 @@ def run_ours(args):
     sl = torch.from_numpy(np.asarray(c["seq_lens"], np.int32)).to(dev)
     max_len = int(np.max(c["seq_lens"]))
     S = mla.resolve_num_splits(args.num_splits, B, Sq, H, max_len)
-    ws_n = mla.workspace_bytes(B, Sq, H, S)
+    ws_n = mla.workspace_bytes(B, Sq, H, S, c["kv"], max_len)
     ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
     q = torch.empty((T, H, mi.D), dtype=torch.bfloat16, device=dev)
     o_lat = torch.empty((B, Sq, H, mi.L), dtype=torch.float32, device=dev)
