@@ -117,6 +117,8 @@ constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 256, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kBarMax = 1, kBarOr = 2, kBarHalf0 = 3;  // named barriers of the softmax warps
+constexpr uint32_t kBarEpi = 4;                             // named barrier of CTA 1's helper warps
+constexpr int kEpiPanelBytes = 128 * 128;                   // 128 rows x 128 B output tile
 
 struct RowGeom {
     int r, s, b, t, j0, j1, npages, page0;
@@ -170,6 +172,7 @@ __device__ __forceinline__ int valid_rows(const RowGeom& g, int page) {
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_sm103_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+                        const __grid_constant__ CUtensorMap o_map,
                         const DecodeArgs p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
@@ -608,45 +611,83 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const float inv = empty ? 0.f : 1.f / l;
             const float lse_v = empty ? -CUDART_INF_F : (m + log2f(lt)) * 0.6931471805599453f;
             const bool live = row < p.H;
-            float* of = nullptr;
-            __nv_bfloat16* ob = nullptr;
-            if (p.num_splits > 1) {
-                of = p.part_o + (((size_t)g.r * p.num_splits + g.s) * p.H + row) * kL;
-                if (live) p.part_lse[((size_t)g.r * p.num_splits + g.s) * p.H + row] = lse_v;
-            } else {
-                if (p.o_dtype == MLA_DT_F32)
-                    of = (float*)p.o_latent + ((size_t)g.r * p.H + row) * kL;
-                else
-                    ob = (__nv_bfloat16*)p.o_latent + ((size_t)g.r * p.H + row) * kL;
-                if (live && p.lse) p.lse[(size_t)g.r * p.H + row] = lse_v;
+            if (live) {
+                const float lse_out = lse_v;
+                if (p.num_splits > 1)
+                    p.part_lse[((size_t)g.r * p.num_splits + g.s) * p.H + row] = lse_out;
+                else if (p.lse)
+                    p.lse[(size_t)g.r * p.H + row] = lse_out;
             }
+            // O / l leaves through TMA stores: each 128-byte-wide column panel of the 128 x 512
+            // result is written to a swizzled shared tile (the V ring is idle now) and stored as
+            // one box of H rows, so that global writes are whole 128-byte lines. fp32 output:
+            // two rounds of eight 32-column panels; bf16: one round of eight 64-column panels.
+            const bool out_f32 = p.num_splits > 1 || p.o_dtype == MLA_DT_F32;
+            const int rounds = out_f32 ? 2 : 1;
+            const int zc = p.num_splits > 1 ? g.r * p.num_splits + g.s : g.r;
+            for (int rd = 0; rd < rounds; ++rd) {
+                if (rd > 0) {  // the previous round's stores have read their tiles
+                    if (ctid == 0) bulk_wait_group_read<0>();
+                    named_bar(kBarEpi, 128);
+                }
 #pragma unroll 1
-            for (int c = 0; c < kL / 32; ++c) {
-                uint32_t v[32];
-                if (use_o) {
-                    tmem_ld32(tmem + lane_base + 32u * c, v);
-                    tmem_wait_ld();
-                } else {
+                for (int pl = 0; pl < 8; ++pl) {
+                    uint8_t* tile = smem + OFF_V + pl * kEpiPanelBytes;
+                    if (out_f32) {
+                        const int col0 = rd * 256 + pl * 32;
+                        uint32_t v[32];
+                        if (use_o) {
+                            tmem_ld32(tmem + lane_base + (uint32_t)col0, v);
+                            tmem_wait_ld();
+                        } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = 0u;
+                            for (int j = 0; j < 32; ++j) v[j] = 0u;
+                        }
+                        if (live) {
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                *reinterpret_cast<uint4*>(tile + row * 128 + ((c ^ (row & 7)) << 4)) = make_uint4(
+                                    __float_as_uint(__uint_as_float(v[4 * c]) * inv),
+                                    __float_as_uint(__uint_as_float(v[4 * c + 1]) * inv),
+                                    __float_as_uint(__uint_as_float(v[4 * c + 2]) * inv),
+                                    __float_as_uint(__uint_as_float(v[4 * c + 3]) * inv));
+                        }
+                    } else {
+                        const int col0 = pl * 64;
+                        uint32_t v[2][32];
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            if (use_o) {
+                                tmem_ld32(tmem + lane_base + (uint32_t)(col0 + 32 * h2), v[h2]);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[h2][j] = 0u;
+                            }
+                        }
+                        if (use_o) tmem_wait_ld();
+                        if (live) {
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                const uint32_t* w = &v[c >> 2][8 * (c & 3)];
+                                *reinterpret_cast<uint4*>(tile + row * 128 + ((c ^ (row & 7)) << 4)) = make_uint4(
+                                    pack_bf16x2(__uint_as_float(w[0]) * inv, __uint_as_float(w[1]) * inv),
+                                    pack_bf16x2(__uint_as_float(w[2]) * inv, __uint_as_float(w[3]) * inv),
+                                    pack_bf16x2(__uint_as_float(w[4]) * inv, __uint_as_float(w[5]) * inv),
+                                    pack_bf16x2(__uint_as_float(w[6]) * inv, __uint_as_float(w[7]) * inv));
+                            }
+                        }
+                    }
                 }
-                if (!live) continue;
-                if (of) {
-                    float4* dst = reinterpret_cast<float4*>(of + 32 * c);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        dst[j] = make_float4(__uint_as_float(v[4 * j]) * inv, __uint_as_float(v[4 * j + 1]) * inv,
-                                             __uint_as_float(v[4 * j + 2]) * inv, __uint_as_float(v[4 * j + 3]) * inv);
-                } else {
-                    uint4* dst = reinterpret_cast<uint4*>(ob + 32 * c);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        dst[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j]) * inv, __uint_as_float(v[8 * j + 1]) * inv),
-                                            pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv, __uint_as_float(v[8 * j + 3]) * inv),
-                                            pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv, __uint_as_float(v[8 * j + 5]) * inv),
-                                            pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv, __uint_as_float(v[8 * j + 7]) * inv));
+                fence_proxy_async_cta();
+                named_bar(kBarEpi, 128);
+                if (ctid == 0) {
+                    const int cpp = out_f32 ? 32 : 64;  // columns per panel
+                    for (int pl = 0; pl < 8; ++pl)
+                        tma_store_3d(&o_map, sbase + OFF_V + pl * kEpiPanelBytes, rd * 256 + pl * cpp, 0, zc);
+                    bulk_commit_group();
                 }
             }
+            if (ctid == 0) bulk_wait_group<0>();  // the stores are complete before the CTA exits
         }
     }
 
@@ -671,9 +712,24 @@ cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         g_attr_done[fp8][dev] = 1;
     }
-    CUtensorMap kv_map, q_map;
+    CUtensorMap kv_map, q_map, o_map;
     memset(&kv_map, 0, sizeof kv_map);
     memset(&q_map, 0, sizeof q_map);
+    memset(&o_map, 0, sizeof o_map);
+    {
+        // output rows [unit][head][512]: the fp32 split partials, or o_latent itself; one box is
+        // one 128-byte-wide column panel of one unit's H rows
+        const bool part = a.num_splits > 1;
+        const bool f32 = part || a.o_dtype == MLA_DT_F32;
+        const uint64_t es = f32 ? 4 : 2;
+        const uint64_t units_o = (uint64_t)a.B * a.Sq * (part ? a.num_splits : 1);
+        const uint64_t dims[3] = {(uint64_t)kL, (uint64_t)a.H, units_o};
+        const uint64_t strides[2] = {(uint64_t)kL * es, (uint64_t)a.H * kL * es};
+        const uint32_t box[3] = {(uint32_t)(128 / es), (uint32_t)a.H, 1u};
+        e = encode_tmap(&o_map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        part ? (const void*)a.part_o : a.o_latent, dims, strides, box, true);
+        if (e != cudaSuccess) return e;
+    }
     if (a.num_blocks > 0 && a.max_seq_len > 0) {
         // bf16 rows of the cache itself, or of the FP8 cache's expanded pages
         const uint64_t rows = fp8 ? (uint64_t)a.B * a.fp8_mp * kPage : (uint64_t)a.num_blocks * kPage;
@@ -689,7 +745,7 @@ cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     const int64_t units = (int64_t)a.B * a.Sq * a.num_splits;
-    kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, s>>>(kv_map, q_map, a);
+    kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, s>>>(kv_map, q_map, o_map, a);
     return cudaGetLastError();
 }
 
