@@ -84,7 +84,13 @@ constexpr int kSmem1 = OFF_PB + kPBufs * kPBufStride;
 constexpr int kSmemBytes = kSmem0 > kSmem1 ? kSmem0 : kSmem1;
 static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
 static_assert(kPMsgBytes % 16 == 0 && kPMsgBytes <= kPBufStride, "P message");
-static_assert(8 * kQPanelBytes == kSlots * kSlotBytes, "Q's latent panels fill the K ring exactly");
+// Q's latent panels land outside ring slots 0 and 1 (so that the first K panels can load at
+// once): panels 0-3 in the P staging area, panels 4-7 in ring slots 2 and 3.
+static_assert(4 * kQPanelBytes <= kPBufs * kPBufStride && 4 * kQPanelBytes == 2 * kSlotBytes, "Q panel homes");
+static_assert(OFF_STAGE % 1024 == 0, "Q panels in the staging area keep the 128-byte swizzle alignment");
+__device__ __forceinline__ uint32_t q_panel_off(int pn) {
+    return pn < 4 ? OFF_STAGE + pn * kQPanelBytes : OFF_RING + 2 * kSlotBytes + (pn - 4) * kQPanelBytes;
+}
 
 // Barrier slots (8 bytes each); one layout for both CTAs so that a multicast commit from CTA 1
 // lands on CTA 0's B_PEMPTY slots.
@@ -220,7 +226,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tma_prefetch_desc(&kv_map);
                 bar_arrive_expect_tx(bar(B_QFULL), 9 * kQPanelBytes);
                 for (int pn = 0; pn < 8; ++pn)
-                    tma_load_2d(sbase + OFF_RING + pn * kQPanelBytes, &q_map, bar(B_QFULL), pn * 64, g.r * p.H);
+                    tma_load_2d(sbase + q_panel_off(pn), &q_map, bar(B_QFULL), pn * 64, g.r * p.H);
                 tma_load_2d(sbase + OFF_QROPE, &q_map, bar(B_QFULL), 8 * 64, g.r * p.H);
                 int issued = 0;  // K panels issued
                 bool ok = true;
@@ -246,8 +252,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     for (int pn = 0; pn < 9; ++pn) {
                         const int m = 9 * gi + pn, slot = m % kSlots, k = m / kSlots;
-                        ok = k == 0 ? wait_bar(bar(B_QREADY), 0, abort, ds)  // Q's panels moved out
-                                    : wait_bar(bar(B_SLOTEMPTY + slot), (k - 1) & 1, abort, ds);
+                        // first use of slots 2 and 3: Q's panels have been moved out to TMEM
+                        ok = k > 0      ? wait_bar(bar(B_SLOTEMPTY + slot), (k - 1) & 1, abort, ds)
+                             : slot >= 2 ? wait_bar(bar(B_QREADY), 0, abort, ds)
+                                         : true;
                         if (!ok) break;
                         const uint32_t full = bar(B_SLOTFULL + slot);
                         const uint32_t dst = sbase + OFF_RING + slot * kSlotBytes;
@@ -319,7 +327,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 8; ++c) {
                         uint4 x = make_uint4(0, 0, 0, 0);
                         if (live && okq)
-                            x = *reinterpret_cast<const uint4*>(smem + OFF_RING + pn * kQPanelBytes + row * 128 +
+                            x = *reinterpret_cast<const uint4*>(smem + q_panel_off(pn) + row * 128 +
                                                                 ((c ^ (row & 7)) << 4));
                         v[4 * c] = x.x;
                         v[4 * c + 1] = x.y;

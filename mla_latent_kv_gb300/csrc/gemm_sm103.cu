@@ -49,7 +49,7 @@ using namespace ptx;
 
 constexpr int kThreads = 320;       // warps 0-3 epilogue, 4 TMA + TMEM, 5 MMA, 6-9 fp32 split
 constexpr int kKChunk = 64;         // K rows per ring stage
-constexpr int kStages = 4;
+constexpr int kStages = 4;          // ring depth (at most; see HeadGemmArgs::stages)
 constexpr int kWBox = 64 * 64 * 2;  // one 64 (m) x 64 (k) bf16 box = 8 KB
 constexpr int kWStage = 2 * kWBox;  // 128 m rows per unit
 constexpr uint32_t kBarConvert = 1; // named barrier of the fp32-split warps
@@ -59,6 +59,7 @@ constexpr int kSlice = 32;          // tokens per epilogue slice (one tcgen05.ld
 struct HeadGemmArgs {
     int T, H, K, M_total;
     int n_tile;              // tokens per unit: multiple of 16, <= 128
+    int stages;              // ring depth, <= kStages
     int x_f32;               // activations fp32 (split into bf16 hi + lo) or bf16
     void* out;               // element (t, h, m) at out[t * out_st + h * out_sh + m]
     int out_f32;
@@ -80,7 +81,7 @@ __device__ __forceinline__ Unit unit_of(int u, int n_tiles, int m_tiles) {
     return r;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     head_gemm_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constant__ CUtensorMap x_map,
                      const __grid_constant__ CUtensorMap o_map, const HeadGemmArgs p) {
     extern __shared__ uint8_t smem_raw[];
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NT = p.n_tile;
+    const int ST = p.stages;
     const int n_tiles = (p.T + NT - 1) / NT;
     const int m_tiles = p.M_total / 128;
     const int units = n_tiles * m_tiles * p.H;
@@ -144,8 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 const Unit w = unit_of(u, n_tiles, m_tiles);
                 for (int c = 0; c < nchunks; ++c, ++g) {
-                    const int s = g % kStages;
-                    if (g >= kStages && !wait_bar(EMPTY(s), ((g / kStages) - 1) & 1, abort_p, nullptr)) {
+                    const int s = g % ST;
+                    if (g >= ST && !wait_bar(EMPTY(s), ((g / ST) - 1) & 1, abort_p, nullptr)) {
                         ok = false;
                         break;
                     }
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) {  // let the copies still in flight land before the CTA leaves
                 int ignore = 0;
                 for (int s = 0; s < kStages; ++s)
-                    if (last[s] >= 0) wait_bar(FULL(s), (last[s] / kStages) & 1, &ignore, nullptr);
+                    if (last[s] >= 0) wait_bar(FULL(s), (last[s] / ST) & 1, &ignore, nullptr);
             }
         }
     } else if (warp == 5) {
@@ -184,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)acc * acc_cols;
                 for (int c = 0; c < nchunks; ++c, ++g) {
-                    const int s = g % kStages;
-                    const uint32_t par = (g / kStages) & 1;
+                    const int s = g % ST;
+                    const uint32_t par = (g / ST) & 1;
                     if (!wait_bar(p.x_f32 ? CONV(s) : FULL(s), par, abort_p, nullptr)) {
                         ok = false;
                         break;
@@ -207,19 +209,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 6) {
         if (!p.x_f32 && p.q_pe != nullptr) {
             // ---- fused concat of the rope part (absorb): q[t, h, 512:576] = q_pe[t, h, :] --
+            // The m tiles of a head share its copy (tile mt takes 16-byte items it with
+            // it % m_tiles == mt); every load of a unit is issued before its stores, so a unit
+            // costs one memory latency.
             const int tid = threadIdx.x - 192;
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
                 const Unit w = unit_of(u, n_tiles, m_tiles);
-                if (w.mt != 0) continue;
-                for (int it = tid; it < NT * 8; it += 128) {
+                constexpr int kMaxItems = 8;  // NT * 8 items / (128 threads) with NT <= 128
+                uint4 v[kMaxItems];
+                int64_t dst[kMaxItems];
+#pragma unroll
+                for (int k = 0; k < kMaxItems; ++k) {
+                    const int it = tid + 128 * k;
                     const int rr = it >> 3, c8 = it & 7;
                     const int t = w.nt * NT + rr;
-                    if (t >= p.T) continue;
-                    const uint4 v = *reinterpret_cast<const uint4*>(p.q_pe + (int64_t)t * p.pe_st +
-                                                                    (int64_t)w.h * p.pe_sh + 8 * c8);
-                    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + (int64_t)t * p.out_st +
-                                              (int64_t)w.h * p.out_sh + kL + 8 * c8) = v;
+                    dst[k] = -1;
+                    if (it < NT * 8 && (it % m_tiles) == w.mt && t < p.T) {
+                        v[k] = *reinterpret_cast<const uint4*>(p.q_pe + (int64_t)t * p.pe_st + (int64_t)w.h * p.pe_sh +
+                                                               8 * c8);
+                        dst[k] = (int64_t)t * p.out_st + (int64_t)w.h * p.out_sh + kL + 8 * c8;
+                    }
                 }
+#pragma unroll
+                for (int k = 0; k < kMaxItems; ++k)
+                    if (dst[k] >= 0) *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + dst[k]) = v[k];
             }
         }
         // ---- fp32 activations -> bf16 hi / lo panels, in place --------------------------
@@ -229,10 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int g = 0;
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
                 for (int c = 0; c < nchunks; ++c, ++g) {
-                    const int s = g % kStages;
+                    const int s = g % ST;
                     // After an abort the wait returns at once; the loop still runs every named
                     // barrier so that no thread of the group is left waiting on another.
-                    wait_bar(FULL(s), (g / kStages) & 1, abort_p, nullptr);
+                    wait_bar(FULL(s), (g / ST) & 1, abort_p, nullptr);
                     uint8_t* const xg = sgen + s * stage_bytes + kWStage;
                     // staged layout: two unswizzled boxes [NT][32] fp32 (k 0-31, k 32-63)
                     uint32_t hw[8][4], lw[8][4];
@@ -273,8 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---- epilogue (warps 0-3): TMEM lane = m, column = token ------------------------
         const int tid = threadIdx.x;
-        const uint32_t stage_base = sbase + kStages * stage_bytes;  // two slice tiles
-        uint8_t* const stage_gen = sgen + kStages * stage_bytes;
+        const uint32_t stage_base = sbase + ST * stage_bytes;  // two slice tiles
+        uint8_t* const stage_gen = sgen + ST * stage_bytes;
         int i = 0, sc = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
             const Unit w = unit_of(u, n_tiles, m_tiles);
@@ -368,11 +381,18 @@ cudaError_t launch_head_gemm(HeadGemmArgs a, const uint16_t* w, const void* x, i
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const int stage_bytes = kWStage + (a.x_f32 ? 2 : 1) * a.n_tile * 128;
-    const int smem = kStages * stage_bytes + 2 * kSlice * 128 * (a.out_f32 ? 4 : 2) + 1024;
+    const int smem = a.stages * stage_bytes + 2 * kSlice * 128 * (a.out_f32 ? 4 : 2) + 1024;
     e = cudaFuncSetAttribute(head_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int units = ((a.T + a.n_tile - 1) / a.n_tile) * (a.M_total / 128) * a.H;
-    const int grid = units < sms ? units : sms;
+    // persistent grid: as many CTAs as fit at once (two per SM when the stages are small, as for
+    // absorb), so that the slowest SM's share of units stays small
+    int per_sm = 1;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, head_gemm_kernel, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const int slots = per_sm * sms;
+    const int grid = units < slots ? units : slots;
     head_gemm_kernel<<<grid, kThreads, smem, s>>>(wmap, xmap, omap, a);
     return cudaGetLastError();
 }
@@ -388,6 +408,7 @@ cudaError_t launch_absorb_sm103(const uint16_t* q_nope, int64_t snt, int64_t snh
     a.K = kP;
     a.M_total = kL;
     a.n_tile = pick_n_tile(T);
+    a.stages = 3;  // small stages: two CTAs share an SM
     a.x_f32 = 0;
     a.out = q_out;
     a.out_f32 = 0;
@@ -407,6 +428,7 @@ cudaError_t launch_out_proj_sm103(const void* o_latent, int in_dtype, const uint
     a.K = kL;
     a.M_total = kV;
     a.n_tile = pick_n_tile(T);
+    a.stages = kStages;
     a.x_f32 = in_dtype == MLA_DT_F32;
     a.out = o;
     a.out_f32 = out_dtype == MLA_DT_F32;
