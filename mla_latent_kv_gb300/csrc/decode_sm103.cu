@@ -217,6 +217,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     cluster_sync();  // both CTAs' barriers exist before any remote arrive or copy
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM);
+    if (tid == 0) griddep_launch_dependents();
 
     if (rank == 0) {
         // ============================== scores CTA ==============================
@@ -224,10 +225,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0 && npages > 0) {
                 tma_prefetch_desc(&q_map);
                 tma_prefetch_desc(&kv_map);
-                bar_arrive_expect_tx(bar(B_QFULL), 9 * kQPanelBytes);
-                for (int pn = 0; pn < 8; ++pn)
-                    tma_load_2d(sbase + q_panel_off(pn), &q_map, bar(B_QFULL), pn * 64, g.r * p.H);
-                tma_load_2d(sbase + OFF_QROPE, &q_map, bar(B_QFULL), 8 * 64, g.r * p.H);
+                // bf16 cache: the first K panels and the L2 prefetch go out before the preceding
+                // kernel (which may be writing q) has finished; the FP8 path's expanded rows are
+                // that kernel's output, so it waits first.
+                if constexpr (kFp8) griddep_wait();
+                bool q_issued = false;
                 int issued = 0;  // K panels issued
                 bool ok = true;
                 // L2 prefetch of whole pages kPrefetchGroups groups ahead of the ring, so that the
@@ -252,6 +254,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     for (int pn = 0; pn < 9; ++pn) {
                         const int m = 9 * gi + pn, slot = m % kSlots, k = m / kSlots;
+                        if (!q_issued && m == 2) {  // Q: the preceding kernel's output
+                            if constexpr (!kFp8) griddep_wait();
+                            bar_arrive_expect_tx(bar(B_QFULL), 9 * kQPanelBytes);
+                            for (int qn = 0; qn < 8; ++qn)
+                                tma_load_2d(sbase + q_panel_off(qn), &q_map, bar(B_QFULL), qn * 64, g.r * p.H);
+                            tma_load_2d(sbase + OFF_QROPE, &q_map, bar(B_QFULL), 8 * 64, g.r * p.H);
+                            q_issued = true;
+                        }
                         // first use of slots 2 and 3: Q's panels have been moved out to TMEM
                         ok = k > 0      ? wait_bar(bar(B_SLOTEMPTY + slot), (k - 1) & 1, abort, ds)
                              : slot >= 2 ? wait_bar(bar(B_QREADY), 0, abort, ds)
@@ -266,7 +276,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (*abort) {  // let the copies in flight land before the CTA can exit
                     volatile int dummy = 0;
-                    wait_bar(bar(B_QFULL), 0, &dummy, nullptr);
+                    if (q_issued) wait_bar(bar(B_QFULL), 0, &dummy, nullptr);
                     for (int m = (issued > kSlots ? issued - kSlots : 0); m < issued; ++m) {
                         dummy = 0;
                         wait_bar(bar(B_SLOTFULL + m % kSlots), (m / kSlots) & 1, &dummy, nullptr);
@@ -503,6 +513,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (warp == 0) {
             if (lane == 0 && npages > 0) {
                 tma_prefetch_desc(&kv_map);
+                if constexpr (kFp8) griddep_wait();  // expanded rows: the preceding kernel's output
                 int issued = 0;
                 for (int i = 0; i < npages; ++i) {
                     const int st = i % kVStages, kv = i / kVStages;
@@ -605,7 +616,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 bar_arrive(bar(B_READY + pb));
                 pages_ready = i + 1;
             }
-            // epilogue
+            // epilogue (outputs may still be read by the preceding kernel until it completes)
+            griddep_wait();
             const bool has_o = npages > 0 && pages_ready == npages && !*abort;
             wait_bar<true>(bar(B_STATS), 0, abort, ds);
             const bool o_ok =
@@ -753,8 +765,7 @@ cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     const int64_t units = (int64_t)a.B * a.Sq * a.num_splits;
-    kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, s>>>(kv_map, q_map, o_map, a);
-    return cudaGetLastError();
+    return launch_pdl(kernel, dim3((unsigned)(2 * units)), dim3(kThreads), kSmemBytes, s, kv_map, q_map, o_map, a);
 }
 
 }  // namespace mla

@@ -38,6 +38,8 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_bytes) {
 }
 
 __global__ void __launch_bounds__(kWarps * 32) fp8_expand_kernel(DecodeArgs p) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();  // it overwrites workspace the preceding kernel may still read
     const int b = blockIdx.x, pg = blockIdx.y;
     int seq = p.seq_lens[b];
     const int cap = p.max_blocks * kPage;
@@ -71,8 +73,7 @@ __global__ void __launch_bounds__(kWarps * 32) fp8_expand_kernel(DecodeArgs p) {
 cudaError_t launch_fp8_expand(const DecodeArgs& a, cudaStream_t s) {
     if (a.B == 0 || a.fp8_mp == 0) return cudaSuccess;
     dim3 grid(a.B, a.fp8_mp);
-    fp8_expand_kernel<<<grid, kWarps * 32, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(fp8_expand_kernel, grid, dim3(kWarps * 32), 0, s, a);
 }
 
 }  // namespace mla

@@ -134,14 +134,31 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     volatile int* abort_p = &abort_flag;
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
     if (warp == 4) {
         // ---- TMA producer ---------------------------------------------------------------
         if (lane == 0) {
             tma_prefetch_desc(&w_map);
             tma_prefetch_desc(&x_map);
-            int g = 0;
+            // The weights of the first unit's first stages go out before the preceding kernel
+            // (which may be writing the activations, or still reading this kernel's output)
+            // has finished; everything else waits for it.
+            const int pre = blockIdx.x < units ? (nchunks < ST ? nchunks : ST) : 0;
             int last[kStages] = {-1, -1, -1, -1};
+            if (pre > 0) {
+                const Unit w0 = unit_of(blockIdx.x, n_tiles, m_tiles);
+                for (int c = 0; c < pre; ++c) {
+                    const uint32_t dst = sbase + c * stage_bytes;
+                    bar_arrive_expect_tx(FULL(c), stage_bytes);
+                    const int wy = w0.h * p.K + c * kKChunk;
+                    tma_load_2d(dst, &w_map, FULL(c), w0.mt * 128, wy);
+                    tma_load_2d(dst + kWBox, &w_map, FULL(c), w0.mt * 128 + 64, wy);
+                    last[c] = c;
+                }
+            }
+            griddep_wait();
+            int g = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 const Unit w = unit_of(u, n_tiles, m_tiles);
@@ -152,10 +169,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                         break;
                     }
                     const uint32_t dst = sbase + s * stage_bytes;
-                    bar_arrive_expect_tx(FULL(s), stage_bytes);
-                    const int wy = w.h * p.K + c * kKChunk;
-                    tma_load_2d(dst, &w_map, FULL(s), w.mt * 128, wy);
-                    tma_load_2d(dst + kWBox, &w_map, FULL(s), w.mt * 128 + 64, wy);
+                    if (g >= pre) {  // the first `pre` stages' weights are already on their way
+                        bar_arrive_expect_tx(FULL(s), stage_bytes);
+                        const int wy = w.h * p.K + c * kKChunk;
+                        tma_load_2d(dst, &w_map, FULL(s), w.mt * 128, wy);
+                        tma_load_2d(dst + kWBox, &w_map, FULL(s), w.mt * 128 + 64, wy);
+                    }
                     if (p.x_f32) {
                         tma_load_3d(dst + kWStage, &x_map, FULL(s), c * kKChunk, w.h, w.nt * NT);
                         tma_load_3d(dst + kWStage + x_panel, &x_map, FULL(s), c * kKChunk + 32, w.h, w.nt * NT);
@@ -213,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // it % m_tiles == mt); every load of a unit is issued before its stores, so a unit
             // costs one memory latency.
             const int tid = threadIdx.x - 192;
+            griddep_wait();
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
                 const Unit w = unit_of(u, n_tiles, m_tiles);
                 constexpr int kMaxItems = 8;  // NT * 8 items / (128 threads) with NT <= 128
@@ -286,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     } else {
         // ---- epilogue (warps 0-3): TMEM lane = m, column = token ------------------------
         const int tid = threadIdx.x;
+        griddep_wait();
         const uint32_t stage_base = sbase + ST * stage_bytes;  // two slice tiles
         uint8_t* const stage_gen = sgen + ST * stage_bytes;
         int i = 0, sc = 0;
@@ -393,8 +414,7 @@ cudaError_t launch_head_gemm(HeadGemmArgs a, const uint16_t* w, const void* x, i
     if (per_sm < 1) per_sm = 1;
     const int slots = per_sm * sms;
     const int grid = units < slots ? units : slots;
-    head_gemm_kernel<<<grid, kThreads, smem, s>>>(wmap, xmap, omap, a);
-    return cudaGetLastError();
+    return launch_pdl(head_gemm_kernel, dim3(grid), dim3(kThreads), (size_t)smem, s, wmap, xmap, omap, a);
 }
 
 }  // namespace

@@ -61,6 +61,25 @@ __host__ __device__ inline void split_range(int n, int S, int s, int* j0, int* j
     *j1 = e < n ? e : n;
 }
 
+// Launch with programmatic stream serialization: the kernel may start while the preceding
+// kernel of the stream finishes, once that kernel has signalled (griddepcontrol); every kernel
+// of this library calls ptx::griddep_wait() before it touches data another of its kernels writes.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Record an error for mla_last_error_detail() and return `st` (printf-style message).
 mla_status set_error(mla_status st, const char* fmt, ...);
 

@@ -11,6 +11,7 @@
 #include <math_constants.h>
 
 #include "internal.h"
+#include "sm103_ptx.cuh"
 
 namespace mla {
 namespace {
@@ -18,6 +19,8 @@ namespace {
 constexpr int kWarps = 8;
 
 __global__ void __launch_bounds__(kWarps * 32) merge_kernel(DecodeArgs p) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();  // the partials are the preceding kernel's output
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int64_t item = (int64_t)blockIdx.x * kWarps + warp;  // (row, head)
     const int64_t n_items = (int64_t)p.B * p.Sq * p.H;
@@ -74,8 +77,7 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(DecodeArgs p) {
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
     const int64_t n_items = (int64_t)a.B * a.Sq * a.H;
     const int64_t blocks = (n_items + kWarps - 1) / kWarps;
-    merge_kernel<<<(unsigned)blocks, kWarps * 32, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(merge_kernel, dim3((unsigned)blocks), dim3(kWarps * 32), 0, s, a);
 }
 
 }  // namespace mla

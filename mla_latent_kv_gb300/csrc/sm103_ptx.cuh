@@ -132,6 +132,18 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 // ------------------------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel of this library signals at its start that the next
+// kernel in the stream may be scheduled; that kernel does its setup and loads only data no
+// kernel of this library writes (weights, KV cache pages, block table), then waits here for
+// the preceding grid to complete (and its memory to be visible) before it reads anything else
+// or writes anything at all.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------------------------
 // TMA (bulk tensor copies global -> shared, completion counted on an mbarrier)
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
