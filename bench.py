@@ -364,9 +364,12 @@ def run_ours(args):
     cpu = None
     if not args.no_cpu_baseline:
         tok_s_cpu, n_items, dt, threads = oracle_sample_rate(c, args.cpu_seconds)
+        n_all = B * Sq * H
+        what = (f"the whole workload (all {n_all} (request, row, head) items)" if n_items >= n_all else
+                f"{n_items} of its {n_all} (request, row, head) items, drawn at random")
         cpu = {"value": tok_s_cpu, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{n_items} random (request, row, head) items of this workload, absorbed fp64 route, "
-                         f"{dt:.1f} s, scaled by H={H} items per token"}
+               "sample": f"{what}, absorbed fp64 route (decode only), {dt:.1f} s, "
+                         f"scaled by H={H} items per token"}
     tokens = T * world
     launches_per_step = 3 + (1 if S > 1 else 0)
     line = {"metric": METRIC, "value": tokens / (step_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
