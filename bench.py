@@ -15,6 +15,7 @@ prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -58,6 +59,21 @@ def load_peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def measured_traffic(workload):
+    """DRAM bytes per decode launch from the committed ncu capture (profiles/traffic.json), or
+    None when that capture was of another workload or of a different decode kernel source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)["decode_sm103.cu"]
+        with open(os.path.join(ROOT, "mla_latent_kv_gb300", "csrc", "decode_sm103.cu"), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("sha256") != h or rec.get("workload") != workload:
+        return None
+    return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
 
 
 def workload_inputs(name, seed_offset=0):
@@ -352,11 +368,11 @@ def run_ours(args):
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs / peaks["hbm_gbs"], "traffic": None}
+                "frac": gbs / peaks["hbm_gbs"], "traffic": measured_traffic(args.workload)}
     else:
         pk = peaks["bf16_tflops_sustained"]
         roof = {"bound": "tensor", "achieved": tflops, "peak": pk, "unit": "TFLOP/s", "frac": tflops / pk,
-                "traffic": None}
+                "traffic": measured_traffic(args.workload)}
     roof.update({"kernel": "mla_decode", "peak_source": f"{peak_src} (MEASURED_PEAKS.json)",
                  "bytes_per_launch": byts, "flops_per_launch": flops,
                  "min_roofline_frac": max(t_hbm, t_tc) / dec_s})
