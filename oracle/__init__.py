@@ -69,6 +69,10 @@ def _load():
                                                   i32, i32, dbl, vp, i64, vp, vp, vp]
         lib.oracle_default_num_splits.restype = i32
         lib.oracle_default_num_splits.argtypes = [i32, i32]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_cache_write.restype = i64
+        lib.oracle_cache_write.argtypes = [vp, i64, vp, i64, vp, i64, i32, ctypes.c_float, vp, i64]
         _lib = lib
         return lib
 
@@ -211,3 +215,23 @@ def out_proj(o_latent, w_uv, T, H):
     out = np.empty((T, H, V), np.float64)
     _load().oracle_out_proj(_ptr(x), _ptr(wv), T, H, _ptr(out))
     return out
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest OCP E4M3 code of the binary32 value x (ties to even, saturating at 448)."""
+    return int(_load().oracle_e4m3_encode(float(x)))
+
+
+def cache_write(kv_c, k_pe, slot_mapping, kv_dtype, cache, num_blocks, kv_scale=0.0):
+    """Write T rows [kv_c || k_pe] (bf16 bit patterns, [T, 512] and [T, 64], rows may be strided
+    views with unit inner stride) into `cache` (uint8, [num_blocks, 64 * row_bytes], modified in
+    place) at slot_mapping (int64, < 0 = skip). Returns the number of out-of-range slots."""
+    kv_c = np.asarray(kv_c)
+    k_pe = np.asarray(k_pe)
+    assert kv_c.dtype == np.uint16 and k_pe.dtype == np.uint16 and cache.dtype == np.uint8
+    assert kv_c.strides[-1] == 2 and k_pe.strides[-1] == 2 and cache.flags.c_contiguous
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    T = slots.shape[0]
+    return int(_load().oracle_cache_write(kv_c.ctypes.data, kv_c.strides[0] // 2 if T else 0, k_pe.ctypes.data,
+                                         k_pe.strides[0] // 2 if T else 0, slots.ctypes.data, T, kv_dtype,
+                                         float(kv_scale), cache.ctypes.data, num_blocks))

@@ -447,3 +447,81 @@ int oracle_default_num_splits(int max_seq_len, int sm_count)
     int cap = 2 * sm_count;
     return p2 < cap ? p2 : cap;
 }
+
+/* ------------------------------------------------------------------------------------------
+ * E4M3 encoding, from the format's definition: the finite value nearest to x, ties to the code
+ * with an even mantissa (round to nearest even), magnitudes beyond the largest finite value
+ * (448) saturate to it, NaN stays NaN. Found by plain search over the 127 non-negative finite
+ * codes, so that nothing but the decoder above is assumed.
+ * ---------------------------------------------------------------------------------------- */
+uint8_t oracle_e4m3_encode(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double err = fabs(oracle_e4m3_value((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* ------------------------------------------------------------------------------------------
+ * KV cache write ([vLLM-MLA, cache write section]): token t's row [kv_c[t] (512) || k_pe[t]
+ * (64)] is stored at slot s = slot_mapping[t] = block * 64 + offset (the block manager's
+ * physical block and in-page offset); s < 0 marks a padding token and is skipped.
+ *   bf16 cache: the 576 bf16 values are copied.
+ *   FP8 cache (584-byte rows, [vLLM-MLA, cache shape and numbers sections]): the row's scale is
+ *   kv_scale when kv_scale > 0 (one static scale, as the page's scale parameter), otherwise
+ *   amax(|x|) / 448 over the row's 576 values (1 when amax is 0). Each value is stored as
+ *   e4m3(x / scale); k_scale (byte 576) and v_scale (byte 580) both hold the scale. The
+ *   division and the rounding decision are taken in binary32, the precision the device uses.
+ * Returns the number of tokens whose slot lies beyond the cache (those rows are skipped).
+ * ---------------------------------------------------------------------------------------- */
+int64_t oracle_cache_write(const uint16_t* kv_c, int64_t st_c, const uint16_t* k_pe, int64_t st_pe,
+                           const int64_t* slot_mapping, int64_t T, int kv_dtype, float kv_scale,
+                           uint8_t* cache, int64_t num_blocks)
+{
+    const int64_t rb = oracle_row_bytes(kv_dtype);
+    int64_t bad = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t s = slot_mapping[t];
+        if (s < 0)
+            continue;
+        if (s >= num_blocks * ORC_PAGE) {
+            ++bad;
+            continue;
+        }
+        uint16_t row[ORC_D];
+        for (int d = 0; d < ORC_L; ++d)
+            row[d] = kv_c[t * st_c + d];
+        for (int r = 0; r < ORC_R; ++r)
+            row[ORC_L + r] = k_pe[t * st_pe + r];
+        uint8_t* dst = cache + s * rb;
+        if (kv_dtype == ORC_KV_BF16) {
+            memcpy(dst, row, sizeof row);
+            continue;
+        }
+        float scale = kv_scale;
+        if (!(scale > 0.0f)) {
+            float amax = 0.0f;
+            for (int d = 0; d < ORC_D; ++d) {
+                const float a = fabsf((float)oracle_bf16_value(row[d]));
+                if (a > amax)
+                    amax = a;
+            }
+            scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        }
+        for (int d = 0; d < ORC_D; ++d)
+            dst[d] = oracle_e4m3_encode((float)oracle_bf16_value(row[d]) / scale);
+        memcpy(dst + ORC_D, &scale, 4);
+        memcpy(dst + ORC_D + 4, &scale, 4);
+    }
+    return bad;
+}

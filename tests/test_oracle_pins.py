@@ -322,3 +322,94 @@ def test_poisoned_rows_are_never_read():
     assert np.isfinite(o).all()
     assert np.isfinite(lse[np.array([oracle.row_len(n, 2, t) > 0 for n in c["seq_lens"]
                                      for t in range(2)]).reshape(4, 2)]).all()
+
+
+# ----------------------------------------------------------------------------- cache write (FP8 quantise)
+def test_e4m3_decoder_known_codes():
+    """OCP E4M3 values fixed by the format: bias 7, 3 mantissa bits, S.1111.111 = NaN."""
+    assert oracle.widen_e4m3([0x38])[0] == 1.0
+    assert oracle.widen_e4m3([0x7E])[0] == 448.0 and oracle.widen_e4m3([0xFE])[0] == -448.0
+    assert oracle.widen_e4m3([0x08])[0] == 2.0 ** -6      # smallest normal
+    assert oracle.widen_e4m3([0x01])[0] == 2.0 ** -9      # smallest subnormal
+    assert oracle.widen_e4m3([0x07])[0] == 7 * 2.0 ** -9  # largest subnormal
+    assert oracle.widen_e4m3([0x39])[0] == 1.125
+    assert np.isnan(oracle.widen_e4m3([0x7F])[0]) and np.isnan(oracle.widen_e4m3([0xFF])[0])
+
+
+def test_e4m3_encoder_round_trip_ties_and_saturation():
+    vals = oracle.widen_e4m3(np.arange(256, dtype=np.uint8))
+    for c in list(range(0, 0x7F)) + list(range(0x80, 0xFF)):   # every finite code, both signs
+        assert oracle.e4m3_encode(np.float32(vals[c])) == c, hex(c)
+    for c in range(0, 0x7E):  # midpoints between neighbours round to the even code
+        lo, hi = vals[c], vals[c + 1]
+        mid = np.float32((lo + hi) / 2)
+        assert float(mid) == (lo + hi) / 2                      # exact in binary32
+        assert oracle.e4m3_encode(mid) == (c if c % 2 == 0 else c + 1), hex(c)
+        assert oracle.e4m3_encode(np.nextafter(mid, np.float32(0))) == c
+        assert oracle.e4m3_encode(np.nextafter(mid, np.float32(1e9))) == c + 1
+        assert oracle.e4m3_encode(-mid) == 0x80 | (c if c % 2 == 0 else c + 1)
+    for big in (449.0, 464.0, 1000.0, 3e38):
+        assert oracle.e4m3_encode(big) == 0x7E and oracle.e4m3_encode(-big) == 0xFE
+    assert oracle.e4m3_encode(2.0 ** -10) == 0x00     # tie between 0 and the smallest subnormal
+    assert oracle.e4m3_encode(0.75 * 2.0 ** -9) == 0x01
+
+
+def _cache_write_case(T, seed, spare=3):
+    rng = np.random.default_rng(seed)
+    kv_c = mi.to_bf16_bits(rng.standard_normal((T, 512)).astype(np.float32) * 2.0)
+    k_pe = mi.to_bf16_bits(rng.standard_normal((T, 64)).astype(np.float32))
+    nb = (T + 63) // 64 + spare
+    slots = rng.permutation(nb * 64)[:T].astype(np.int64)
+    return kv_c, k_pe, slots, nb
+
+
+def test_cache_write_bf16_rows_land_at_their_slots():
+    T = 70
+    kv_c, k_pe, slots, nb = _cache_write_case(T, 70)
+    slots[5] = -1                       # padding token
+    slots[9] = nb * 64 + 3              # beyond the cache: counted, skipped
+    cache = np.full((nb, 64 * 1152), 0xAB, np.uint8)
+    assert oracle.cache_write(kv_c, k_pe, slots, oracle.KV_BF16, cache, nb) == 1
+    rows = cache.reshape(nb * 64, 1152)
+    for t in range(T):
+        if t in (5, 9):
+            continue
+        expect = np.concatenate([kv_c[t], k_pe[t]]).view(np.uint8)
+        np.testing.assert_array_equal(rows[slots[t]], expect)
+    written = set(int(s) for i, s in enumerate(slots) if i not in (5, 9))
+    untouched = [r for r in range(nb * 64) if r not in written]
+    assert np.all(rows[untouched] == 0xAB)
+
+
+@pytest.mark.parametrize("kv_scale", [0.0, 0.05, 1.0])
+def test_cache_write_fp8_quantises_per_definition(kv_scale):
+    T = 40
+    kv_c, k_pe, slots, nb = _cache_write_case(T, 71)
+    kv_c[3] = 0                                   # an all-zero latent ...
+    k_pe[3] = 0                                   # ... and rope: amax 0 -> scale 1
+    cache = np.zeros((nb, 64 * 584), np.uint8)
+    assert oracle.cache_write(kv_c, k_pe, slots, oracle.KV_FP8, cache, nb, kv_scale=kv_scale) == 0
+    rows = cache.reshape(nb * 64, 584)
+    for t in range(T):
+        r = rows[slots[t]]
+        x = oracle.widen_bf16(np.concatenate([kv_c[t], k_pe[t]]))
+        ks = r[576:580].copy().view(np.float32)[0]
+        vs = r[580:584].copy().view(np.float32)[0]
+        assert ks == vs
+        if kv_scale > 0:
+            assert ks == np.float32(kv_scale)
+        elif t == 3:
+            assert ks == 1.0 and np.all(r[:576] == 0)
+            continue
+        else:
+            amax = np.float32(np.max(np.abs(x)))
+            assert ks == np.float32(amax / np.float32(448.0))
+            assert np.any((r[:576] & 0x7F) == 0x7E)          # the largest element maps to +-448
+        deq = oracle.widen_e4m3(r[:576]) * float(ks)
+        q = x / float(ks)
+        inside = np.abs(q) <= 448
+        # within half an e4m3 step of the exact quotient: 2^-4 relative for normals, 2^-10
+        # absolute in the subnormal range; saturated values sit at +-448
+        err = np.abs(deq[inside] / float(ks) - q[inside])
+        assert np.all(err <= np.maximum(np.abs(q[inside]) * 2.0 ** -4, 2.0 ** -10) + 1e-12)
+        assert np.all(np.abs(deq[~inside] / float(ks)) == 448.0)
