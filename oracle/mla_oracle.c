@@ -479,9 +479,11 @@ uint8_t oracle_e4m3_encode(float x)
  *   bf16 cache: the 576 bf16 values are copied.
  *   FP8 cache (584-byte rows, [vLLM-MLA, cache shape and numbers sections]): the row's scale is
  *   kv_scale when kv_scale > 0 (one static scale, as the page's scale parameter), otherwise
- *   amax(|x|) / 448 over the row's 576 values (1 when amax is 0). Each value is stored as
- *   e4m3(x / scale); k_scale (byte 576) and v_scale (byte 580) both hold the scale. The
- *   division and the rounding decision are taken in binary32, the precision the device uses.
+ *   amax(|x|) / 448 over the row's 576 values (1 when amax is 0). The write multiplies each
+ *   value by the scale's reciprocal ([vLLM-MLA, cache write section]: with a scale of exactly 1
+ *   the multiplication is the step that can be skipped) and stores e4m3(x * (1 / scale));
+ *   k_scale (byte 576) and v_scale (byte 580) both hold the scale. amax / 448, 1 / scale, the
+ *   product and the rounding decision are all taken in binary32, the precision the device uses.
  * Returns the number of tokens whose slot lies beyond the cache (those rows are skipped).
  * ---------------------------------------------------------------------------------------- */
 int64_t oracle_cache_write(const uint16_t* kv_c, int64_t st_c, const uint16_t* k_pe, int64_t st_pe,
@@ -518,8 +520,9 @@ int64_t oracle_cache_write(const uint16_t* kv_c, int64_t st_c, const uint16_t* k
             }
             scale = amax > 0.0f ? amax / 448.0f : 1.0f;
         }
+        const float inv = 1.0f / scale;
         for (int d = 0; d < ORC_D; ++d)
-            dst[d] = oracle_e4m3_encode((float)oracle_bf16_value(row[d]) / scale);
+            dst[d] = oracle_e4m3_encode((float)oracle_bf16_value(row[d]) * inv);
         memcpy(dst + ORC_D, &scale, 4);
         memcpy(dst + ORC_D + 4, &scale, 4);
     }

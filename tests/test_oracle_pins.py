@@ -406,7 +406,7 @@ def test_cache_write_fp8_quantises_per_definition(kv_scale):
             assert ks == np.float32(amax / np.float32(448.0))
             assert np.any((r[:576] & 0x7F) == 0x7E)          # the largest element maps to +-448
         deq = oracle.widen_e4m3(r[:576]) * float(ks)
-        q = x / float(ks)
+        q = (x.astype(np.float32) * (np.float32(1.0) / ks)).astype(np.float64)  # x * (1 / scale), binary32
         inside = np.abs(q) <= 448
         # within half an e4m3 step of the exact quotient: 2^-4 relative for normals, 2^-10
         # absolute in the subnormal range; saturated values sit at +-448
