@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dsv3", choices=sorted(mi.WORKLOADS))
+    ap.add_argument("--component", default="step", choices=["step", "cache_write"],
+                    help="step: absorb -> decode -> out_proj (the hot path); cache_write: the KV cache "
+                         "write that precedes it, measured alone (FP8 quantise for the fp8 workload)")
     ap.add_argument("--num-splits", type=int, default=-1,
                     help="-1: GB300 planner, 0: the pages' Triton rule, >0 forced")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline sample budget")
@@ -406,10 +409,60 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_cache_write(args):
+    """mla_cache_write on one prefill-sized chunk of new tokens (65536 rows) of the workload's
+    cache format; HBM-bound: 1152 bytes read and row_bytes written per token."""
+    import torch
+    import mla_latent_kv_gb300 as mla
+    mla.lib()
+    dev = torch.device("cuda", 0)
+    kv = mi.WORKLOADS[args.workload]["kv"]
+    T = 65536
+    rng = np.random.default_rng(7)
+    nb = T // 64 + 16
+    kv_c = torch.randn(T, 512, device=dev).bfloat16()
+    k_pe = torch.randn(T, 64, device=dev).bfloat16()
+    slots = torch.from_numpy(rng.permutation(nb * 64)[:T].astype(np.int64)).to(dev)
+    rb = mi.ROW_BYTES[kv]
+    cache = torch.zeros(nb, 64 * rb, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(args.flush_mb * (1 << 20), dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        mla.cache_write(kv_c, k_pe, slots, cache, kv_dtype=kv, dev_status=status)
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(None)
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        mla.cache_write(kv_c, k_pe, slots, cache, kv_dtype=kv, dev_status=status)
+        b.record()
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    assert int(status.item()) == 0
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    byts = T * (1152 + rb + 8)  # rows read, rows written, slot ids
+    peaks, src = load_peaks()
+    gbs = byts / (ms * 1e-3) / 1e9
+    line = {"metric": "KV cache write tokens/s", "value": T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+            "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8" if kv == mi.KV_FP8 else "bf16", "data": "synthetic",
+            "config": {"workload": f"cache_write: {T} new tokens into a {'584' if kv else '1152'}-byte-row cache",
+                       "l2": f"{args.flush_mb} MB L2 flush between launches"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "mla_cache_write",
+                         "bytes_per_launch": byts, "peak_source": f"{src} (MEASURED_PEAKS.json)"},
+            "gpu_launches": K, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.component == "cache_write":
+        run_cache_write(args)
     else:
         run_ours(args)
 

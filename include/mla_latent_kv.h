@@ -73,6 +73,7 @@ typedef enum { MLA_DT_F32 = 0, MLA_DT_BF16 = 1 } mla_dtype;
 #define MLA_DEV_BAD_BLOCK_ID 0x1 /* a needed block_table entry was outside [0, num_blocks) */
 #define MLA_DEV_SEQ_TOO_LONG 0x2 /* seq_lens[b] > max_blocks * 64 or > max_seq_len */
 #define MLA_DEV_WAIT_TIMEOUT 0x4 /* a bounded pipeline wait expired; outputs are invalid */
+#define MLA_DEV_BAD_SLOT 0x8     /* mla_cache_write: a slot at or beyond num_blocks * 64 (skipped) */
 
 /* Human-readable name of a status. Never NULL. */
 const char* mla_status_string(mla_status s);
@@ -183,6 +184,29 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
  */
 mla_status mla_out_proj(const void* o_latent, mla_dtype in_dtype, const void* W_UV, void* o,
                         mla_dtype out_dtype, int T, int H, mla_stream_t stream);
+
+/*
+ * KV cache write, the step before decode ([vLLM-MLA, cache write section]: the latent and k_pe
+ * land in the cache in one kernel, at the slot the block manager assigned each token). Token t's
+ * row [kv_c[t, 0:512] || k_pe[t, 0:64]] goes to slot s = slot_mapping[t] = block * 64 + in-page
+ * offset of kv_cache; s < 0 marks a padding token and is skipped.
+ *   MLA_KV_BF16             the 576 bf16 values are copied (1152-byte row).
+ *   MLA_KV_FP8_E4M3_SCALED  every value is stored as e4m3(x * (1 / scale)), rounded to nearest
+ *                           even and saturated at +-448, with scale = kv_scale when kv_scale > 0
+ *                           (one static scale, as vLLM's per-layer scale), else amax(|row|) / 448
+ *                           over the row's 576 values (1 for an all-zero row); amax / 448, the
+ *                           reciprocal and the product are binary32, each correctly rounded. k_scale (byte 576) and v_scale (byte 580) both
+ *                           receive the scale ([vLLM-MLA, cache shape and numbers sections]).
+ *   kv_c          bf16, element (t, d) at kv_c[t * kv_c_stride_t + d]   (stride % 8 == 0)
+ *   k_pe          bf16, element (t, r) at k_pe[t * k_pe_stride_t + r]   (stride % 8 == 0)
+ *   slot_mapping  int64 [T] in device memory
+ *   kv_cache      [num_blocks, 64, mla_kv_row_bytes(kv_dtype)] bytes, 16-byte aligned
+ * A slot at or beyond num_blocks * 64 sets MLA_DEV_BAD_SLOT in *dev_status (if given) and the
+ * token is skipped. T >= 0 (T == 0 launches nothing). Pointers 16-byte aligned.
+ */
+mla_status mla_cache_write(const void* kv_c, int64_t kv_c_stride_t, const void* k_pe, int64_t k_pe_stride_t,
+                           const int64_t* slot_mapping, int T, void* kv_cache, mla_kv_dtype kv_dtype,
+                           int64_t num_blocks, float kv_scale, int32_t* dev_status, mla_stream_t stream);
 
 /*
  * mla_decode without a workspace argument, for callers that cannot allocate device memory when

@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         l.mla_decode_noalloc.restype = i32
         l.mla_decode_noalloc.argtypes = [vp, vp, i32, i64, vp, i32, vp, i32, i32, i32, i32, f32, i32, vp, i32,
                                          vp, vp, vp]
+        l.mla_cache_write.restype = i32
+        l.mla_cache_write.argtypes = [vp, i64, vp, i64, vp, i32, vp, i32, i64, f32, vp, vp]
         l.mla_out_proj.restype = i32
         l.mla_out_proj.argtypes = [vp, i32, vp, vp, i32, i32, i32, vp]
         _lib = l
@@ -187,6 +189,19 @@ def decode_noalloc(q, kv_cache, block_table, seq_lens, max_seq_len, scale, kv_dt
                                     int(num_splits), _p(o_latent), o_dtype, _p(lse), _p(dev_status),
                                     _stream(stream)))
     return o_latent, lse
+
+
+def cache_write(kv_c, k_pe, slot_mapping, kv_cache, kv_dtype=KV_BF16, kv_scale=0.0, dev_status=None, stream=None,
+                num_blocks=None):
+    """kv_c [T, 512] bf16 and k_pe [T, 64] bf16 (rows may be strided, unit inner stride),
+    slot_mapping [T] int64 (< 0 = padding) -> rows written into kv_cache in place."""
+    T = int(slot_mapping.shape[0])
+    if num_blocks is None:
+        num_blocks = kv_cache.numel() * kv_cache.element_size() // (PAGE * row_bytes(kv_dtype))
+    _check(lib().mla_cache_write(_p(kv_c), kv_c.stride(0) if T else L, _p(k_pe), k_pe.stride(0) if T else R,
+                                 _p(slot_mapping), T, _p(kv_cache), kv_dtype, int(num_blocks), float(kv_scale),
+                                 _p(dev_status), _stream(stream)))
+    return kv_cache
 
 
 def out_proj(o_latent, w_uv, out=None, out_dtype=DT_F32, stream=None):

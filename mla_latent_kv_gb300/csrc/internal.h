@@ -86,6 +86,9 @@ mla_status set_error(mla_status st, const char* fmt, ...);
 cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_fp8_expand(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_cache_write(const uint16_t* kv_c, int64_t st_c, const uint16_t* k_pe, int64_t st_pe,
+                               const int64_t* slots, int T, uint8_t* cache, int kv_dtype, int64_t num_blocks,
+                               float kv_scale, int32_t* dev_status, cudaStream_t s);
 cudaError_t launch_absorb_sm103(const uint16_t* q_nope, int64_t snt, int64_t snh, const uint16_t* q_pe,
                                 int64_t spt, int64_t sph, const uint16_t* w_uk_t, uint16_t* q_out, int T, int H,
                                 cudaStream_t s);

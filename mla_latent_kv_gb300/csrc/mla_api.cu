@@ -262,6 +262,29 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
     return ok();
 }
 
+mla_status mla_cache_write(const void* kv_c, int64_t kv_c_stride_t, const void* k_pe, int64_t k_pe_stride_t,
+                           const int64_t* slot_mapping, int T, void* kv_cache, mla_kv_dtype kv_dtype,
+                           int64_t num_blocks, float kv_scale, int32_t* dev_status, mla_stream_t stream) {
+    if (T < 0) return fail(MLA_ERR_INVALID_ARG, "mla_cache_write: T=%d < 0", T);
+    if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3_SCALED)
+        return fail(MLA_ERR_INVALID_ARG, "mla_cache_write: unknown kv_dtype %d", (int)kv_dtype);
+    if (num_blocks < 0) return fail(MLA_ERR_INVALID_ARG, "mla_cache_write: num_blocks < 0");
+    if (!(kv_scale >= 0.f) || std::isinf(kv_scale))
+        return fail(MLA_ERR_INVALID_ARG, "mla_cache_write: kv_scale must be finite and >= 0 (0 = per-token)");
+    if (T == 0) return ok();
+    if (!kv_c || !k_pe || !slot_mapping || !kv_cache) return fail(MLA_ERR_INVALID_ARG, "mla_cache_write: null pointer");
+    if (!aligned16(kv_c) || !aligned16(k_pe) || !aligned16(kv_cache))
+        return fail(MLA_ERR_UNSUPPORTED, "mla_cache_write: kv_c, k_pe and kv_cache must be 16-byte aligned");
+    if (kv_c_stride_t < mla::kL || k_pe_stride_t < mla::kR || kv_c_stride_t % 8 || k_pe_stride_t % 8)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_cache_write: row strides must be multiples of 8 covering the row");
+    if (num_blocks > (int64_t)1 << 40) return fail(MLA_ERR_UNSUPPORTED, "mla_cache_write: num_blocks too large");
+    cudaError_t e = mla::launch_cache_write((const uint16_t*)kv_c, kv_c_stride_t, (const uint16_t*)k_pe,
+                                            k_pe_stride_t, slot_mapping, T, (uint8_t*)kv_cache, kv_dtype,
+                                            num_blocks, kv_scale, dev_status, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "mla_cache_write launch");
+    return ok();
+}
+
 mla_status mla_out_proj(const void* o_latent, mla_dtype in_dtype, const void* W_UV, void* o, mla_dtype out_dtype,
                         int T, int H, mla_stream_t stream) {
     if (T < 0) return fail(MLA_ERR_INVALID_ARG, "mla_out_proj: T=%d < 0", T);
