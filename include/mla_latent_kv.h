@@ -96,13 +96,21 @@ int mla_default_num_splits(int max_seq_len, int sm_count);
  *           -1  this library's own choice for GB300: the smallest count whose grid of
  *               (B*Sq*splits) units fills whole waves of the device's SMs, capped by the
  *               number of 64-token pages of the longest row.
+ *           -2  no uniform count: a schedule is built on the device from seq_lens (no host
+ *               synchronisation, [vLLM-MLA, metadata section]: FlashMLA's decode metadata
+ *               carries a scheduler plan). Every query row is cut into page-aligned units of
+ *               about c pages, with c chosen from the total and longest row lengths by a model
+ *               of how the device's 2-SM clusters run the units; a row that gets one unit writes
+ *               its output directly. For batches whose lengths differ widely. Returned as -2.
  * Returns -1 on invalid arguments or if the SM count cannot be queried. Host only, no sync. */
 int mla_resolve_num_splits(int num_splits, int B, int Sq, int H, int max_seq_len);
 
 /* Bytes of split-KV workspace mla_decode needs for `num_splits` resolved splits: 0 when
  * num_splits == 1, else B*Sq*num_splits*H*(512 + 1)*4 rounded up to 256 (fp32 partial outputs
  * and partial LSEs, [vLLM-MLA, Triton MLA section]: attn_logits (B, N, splits, 512 + 1), fp32
- * because the LSE precision decides the merge). Host only. */
+ * because the LSE precision decides the merge). num_splits == -2 (device-built schedule): the
+ * schedule (256 B + 16 B per unit + 8 B per query row) and partials for B*Sq + SMs units, each
+ * region 256-byte aligned. Host only. */
 size_t mla_decode_workspace_bytes(int B, int Sq, int H, int num_splits);
 
 /* Bytes of workspace mla_decode needs for a cache of format kv_dtype (valid for both formats;

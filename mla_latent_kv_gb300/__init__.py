@@ -101,7 +101,7 @@ def default_num_splits(max_seq_len: int, sm_count: int) -> int:
 
 def resolve_num_splits(num_splits: int, B: int, Sq: int, H: int, max_seq_len: int) -> int:
     s = int(lib().mla_resolve_num_splits(num_splits, B, Sq, H, max_seq_len))
-    if s < 1:
+    if s < 1 and s != -2:  # -2: per-row schedule built on the device
         raise MlaError(ERR_INVALID_ARG, "could not resolve num_splits")
     return s
 

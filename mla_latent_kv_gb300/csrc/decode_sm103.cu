@@ -127,25 +127,26 @@ constexpr uint32_t kBarEpi = 4;                             // named barrier of 
 constexpr int kEpiPanelBytes = 128 * 128;                   // 128 rows x 128 B output tile
 
 struct RowGeom {
-    int r, s, b, t, j0, j1, npages, page0;
+    int r, b, t, j0, j1, npages, page0;
+    int slot;  // partial-output slot, or -1: this unit writes the row's final output
 };
 
 __device__ __forceinline__ RowGeom row_geometry(const DecodeArgs& p, int unit, bool report) {
     RowGeom g;
-    g.r = unit / p.num_splits;
-    g.s = unit % p.num_splits;
+    if (p.plan_units) {  // device-built schedule
+        const int4 u = p.plan_units[unit];
+        g.r = u.x;
+        g.j0 = u.y;
+        g.j1 = u.z;
+        g.slot = u.w;
+    } else {  // uniform splits: unit = row * S + split
+        const int S = p.num_splits;
+        g.r = unit / S;
+        split_range(visible_tokens(p, g.r, report), S, unit % S, &g.j0, &g.j1);
+        g.slot = S > 1 ? unit : -1;
+    }
     g.b = g.r / p.Sq;
     g.t = g.r % p.Sq;
-    int seq = p.seq_lens[g.b];
-    // FP8 cache: the expanded layout holds fp8_mp pages per request
-    const int cap = (p.fp8_mp > 0 && p.fp8_mp < p.max_blocks ? p.fp8_mp : p.max_blocks) * kPage;
-    if (seq > cap || seq > p.max_seq_len || seq < 0) {
-        if (report && p.dev_status) atomicOr(p.dev_status, MLA_DEV_SEQ_TOO_LONG);
-        seq = seq < 0 ? 0 : (seq > cap ? cap : seq);
-    }
-    int n = seq - (p.Sq - 1 - g.t);
-    if (n < 0) n = 0;
-    split_range(n, p.num_splits, g.s, &g.j0, &g.j1);
     g.npages = (g.j1 - g.j0 + kPage - 1) / kPage;
     g.page0 = g.j0 / kPage;
     return g;
@@ -178,7 +179,7 @@ __device__ __forceinline__ int valid_rows(const RowGeom& g, int page) {
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_sm103_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
-                        const __grid_constant__ CUtensorMap o_map,
+                        const __grid_constant__ CUtensorMap o_map, const __grid_constant__ CUtensorMap p_map,
                         const DecodeArgs p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
@@ -189,6 +190,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         return;  // both CTAs of the cluster see the same alignment and leave together
     }
     const int unit = (int)(blockIdx.x >> 1);
+    if (p.plan_units) {
+        // the schedule is the preceding kernel's output; clusters past its unit count leave
+        // together (both CTAs read the same count) before touching anything
+        griddep_wait();
+        if (unit >= *p.plan_count) return;
+    }
     const RowGeom g = row_geometry(p, unit, tid == 0 && rank == 0);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
     int32_t* ds = p.dev_status;
@@ -633,8 +640,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const bool live = row < p.H;
             if (live) {
                 const float lse_out = lse_v;
-                if (p.num_splits > 1)
-                    p.part_lse[((size_t)g.r * p.num_splits + g.s) * p.H + row] = lse_out;
+                if (g.slot >= 0)
+                    p.part_lse[(size_t)g.slot * p.H + row] = lse_out;
                 else if (p.lse)
                     p.lse[(size_t)g.r * p.H + row] = lse_out;
             }
@@ -642,9 +649,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // result is written to a swizzled shared tile (the V ring is idle now) and stored as
             // one box of H rows, so that global writes are whole 128-byte lines. fp32 output:
             // two rounds of eight 32-column panels; bf16: one round of eight 64-column panels.
-            const bool out_f32 = p.num_splits > 1 || p.o_dtype == MLA_DT_F32;
+            const bool out_f32 = g.slot >= 0 || p.o_dtype == MLA_DT_F32;
             const int rounds = out_f32 ? 2 : 1;
-            const int zc = p.num_splits > 1 ? g.r * p.num_splits + g.s : g.r;
+            const int zc = g.slot >= 0 ? g.slot : g.r;
+            const CUtensorMap* omap = g.slot >= 0 ? &p_map : &o_map;
             for (int rd = 0; rd < rounds; ++rd) {
                 if (rd > 0) {  // the previous round's stores have read their tiles
                     if (ctid == 0) bulk_wait_group_read<0>();
@@ -703,7 +711,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (ctid == 0) {
                     const int cpp = out_f32 ? 32 : 64;  // columns per panel
                     for (int pl = 0; pl < 8; ++pl)
-                        tma_store_3d(&o_map, sbase + OFF_V + pl * kEpiPanelBytes, rd * 256 + pl * cpp, 0, zc);
+                        tma_store_3d(omap, sbase + OFF_V + pl * kEpiPanelBytes, rd * 256 + pl * cpp, 0, zc);
                     bulk_commit_group();
                 }
             }
@@ -732,22 +740,31 @@ cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         g_attr_done[fp8][dev] = 1;
     }
-    CUtensorMap kv_map, q_map, o_map;
+    CUtensorMap kv_map, q_map, o_map, p_map;
     memset(&kv_map, 0, sizeof kv_map);
     memset(&q_map, 0, sizeof q_map);
     memset(&o_map, 0, sizeof o_map);
+    memset(&p_map, 0, sizeof p_map);
+    const bool planned = a.plan_units != nullptr;
+    const int64_t units = planned ? a.plan_max_units : (int64_t)a.B * a.Sq * a.num_splits;
     {
-        // output rows [unit][head][512]: the fp32 split partials, or o_latent itself; one box is
-        // one 128-byte-wide column panel of one unit's H rows
-        const bool part = a.num_splits > 1;
-        const bool f32 = part || a.o_dtype == MLA_DT_F32;
+        // final rows [row][head][512] of o_latent; one box is one 128-byte-wide column panel
+        // of one row's H heads
+        const bool f32 = a.o_dtype == MLA_DT_F32;
         const uint64_t es = f32 ? 4 : 2;
-        const uint64_t units_o = (uint64_t)a.B * a.Sq * (part ? a.num_splits : 1);
-        const uint64_t dims[3] = {(uint64_t)kL, (uint64_t)a.H, units_o};
+        const uint64_t dims[3] = {(uint64_t)kL, (uint64_t)a.H, (uint64_t)a.B * a.Sq};
         const uint64_t strides[2] = {(uint64_t)kL * es, (uint64_t)a.H * kL * es};
         const uint32_t box[3] = {(uint32_t)(128 / es), (uint32_t)a.H, 1u};
         e = encode_tmap(&o_map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                        part ? (const void*)a.part_o : a.o_latent, dims, strides, box, true);
+                        a.o_latent, dims, strides, box, true);
+        if (e != cudaSuccess) return e;
+    }
+    if (a.part_o) {
+        // fp32 partial rows [slot][head][512] of the split units
+        const uint64_t dims[3] = {(uint64_t)kL, (uint64_t)a.H, (uint64_t)units};
+        const uint64_t strides[2] = {(uint64_t)kL * 4, (uint64_t)a.H * kL * 4};
+        const uint32_t box[3] = {32u, (uint32_t)a.H, 1u};
+        e = encode_tmap(&p_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.part_o, dims, strides, box, true);
         if (e != cudaSuccess) return e;
     }
     if (a.num_blocks > 0 && a.max_seq_len > 0) {
@@ -764,8 +781,8 @@ cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s) {
         e = encode_tmap(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, qdims, strides, qbox, true);
         if (e != cudaSuccess) return e;
     }
-    const int64_t units = (int64_t)a.B * a.Sq * a.num_splits;
-    return launch_pdl(kernel, dim3((unsigned)(2 * units)), dim3(kThreads), kSmemBytes, s, kv_map, q_map, o_map, a);
+    return launch_pdl(kernel, dim3((unsigned)(2 * units)), dim3(kThreads), kSmemBytes, s, kv_map, q_map, o_map,
+                      p_map, a);
 }
 
 }  // namespace mla

@@ -18,17 +18,36 @@ namespace {
 
 constexpr int kWarps = 8;
 
+__device__ __forceinline__ void merge_item(const DecodeArgs& p, int64_t r, int h, int lane);
+
 __global__ void __launch_bounds__(kWarps * 32) merge_kernel(DecodeArgs p) {
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();  // the partials are the preceding kernel's output
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int64_t item = (int64_t)blockIdx.x * kWarps + warp;  // (row, head)
     const int64_t n_items = (int64_t)p.B * p.Sq * p.H;
-    if (item >= n_items) return;
-    const int64_t r = item / p.H;
-    const int h = (int)(item % p.H);
-    const int S = p.num_splits;
-    const float* lse_p = p.part_lse + (size_t)r * S * p.H + h;  // stride H between splits
+    // grid-stride over (row, head); with a device-built schedule most rows have no partials
+    // and their items are skipped after one load
+    for (int64_t item = (int64_t)blockIdx.x * kWarps + warp; item < n_items; item += (int64_t)gridDim.x * kWarps) {
+        const int64_t r = item / p.H;
+        if (p.plan_rows && p.plan_rows[r].y <= 1) continue;  // the row wrote its output directly
+        merge_item(p, r, (int)(item % p.H), lane);
+    }
+}
+
+__device__ __forceinline__ void merge_item(const DecodeArgs& p, int64_t r, int h, int lane) {
+    // the row's partials are slots [slot0, slot0 + S): uniform splits put row r at r * S; a
+    // device-built schedule lists them per row (a row with one unit already wrote its output)
+    int S, slot0;
+    if (p.plan_rows) {
+        const int2 ri = p.plan_rows[r];
+        S = ri.y;
+        slot0 = ri.x;
+        if (S <= 1) return;
+    } else {
+        S = p.num_splits;
+        slot0 = (int)(r * S);
+    }
+    const float* lse_p = p.part_lse + (size_t)slot0 * p.H + h;  // stride H between splits
 
     float M = -CUDART_INF_F;
     for (int s = lane; s < S; s += 32) M = fmaxf(M, lse_p[(size_t)s * p.H]);
@@ -46,7 +65,7 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(DecodeArgs p) {
             const float w = __expf(ls - M);
             wsum += w;
             const float4* src = reinterpret_cast<const float4*>(
-                p.part_o + (((size_t)r * S + s) * p.H + h) * kL + lane * 16);
+                p.part_o + (((size_t)slot0 + s) * p.H + h) * kL + lane * 16);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 float4 v = src[i];
@@ -76,7 +95,8 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(DecodeArgs p) {
 
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
     const int64_t n_items = (int64_t)a.B * a.Sq * a.H;
-    const int64_t blocks = (n_items + kWarps - 1) / kWarps;
+    int64_t blocks = (n_items + kWarps - 1) / kWarps;
+    if (a.plan_rows && blocks > 1216) blocks = 1216;  // grid-stride; the split rows are few
     return launch_pdl(merge_kernel, dim3((unsigned)blocks), dim3(kWarps * 32), 0, s, a);
 }
 

@@ -53,11 +53,20 @@ WorkspaceLayout workspace_layout(int kv_dtype, int B, int Sq, int H, int num_spl
     WorkspaceLayout w{};
     if (B <= 0 || Sq <= 0 || H <= 0) return w;
     size_t off = 0;
-    if (num_splits > 1) {
-        const size_t units = (size_t)B * Sq * num_splits * H;
-        w.part_o = 0;
-        w.part_lse = up(units * kL * sizeof(float));
+    int64_t slots = num_splits > 1 ? (int64_t)B * Sq * num_splits : 0;
+    if (num_splits == -2) {  // device-built schedule: header, unit list, per-row slots
+        const int sms = device_sm_count();
+        if (sms < 1) return w;
+        slots = plan_max_units((int64_t)B * Sq, sms / 2 > 0 ? sms / 2 : 1);
+        w.plan = 0;
+        off = up(256 + (size_t)slots * sizeof(int4)) + up((size_t)B * Sq * sizeof(int2));
+    }
+    if (slots > 0) {
+        const size_t units = (size_t)slots * H;
+        w.part_o = off;
+        w.part_lse = off + up(units * kL * sizeof(float));
         off = w.part_lse + up(units * sizeof(float));
+        w.partial_slots = slots;
     }
     if (kv_dtype == MLA_KV_FP8_E4M3_SCALED && max_seq_len > 0) {
         const size_t rows = (size_t)B * ((max_seq_len + kPage - 1) / kPage) * kPage;
@@ -112,7 +121,8 @@ int mla_default_num_splits(int max_seq_len, int sm_count) {
 
 int mla_resolve_num_splits(int num_splits, int B, int Sq, int H, int max_seq_len) {
     if (num_splits > 0) return num_splits;
-    if (num_splits < -1 || B < 0 || Sq < 1 || H < 1 || max_seq_len < 0) return -1;
+    if (num_splits < -2 || B < 0 || Sq < 1 || H < 1 || max_seq_len < 0) return -1;
+    if (num_splits == -2) return device_sm_count() >= 1 ? -2 : -1;  // decided per row on the device
     int sms = device_sm_count();
     if (sms < 1) return -1;
     if (num_splits == 0) return mla_default_num_splits(max_seq_len, sms);
@@ -192,7 +202,7 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
                     (long long)max_blocks * mla::kPage);
     if (!(std::isfinite(scale)) || scale <= 0.f)
         return fail(MLA_ERR_INVALID_ARG, "mla_decode: scale must be finite and > 0");
-    if (num_splits < -1) return fail(MLA_ERR_INVALID_ARG, "mla_decode: num_splits=%d < -1", num_splits);
+    if (num_splits < -2) return fail(MLA_ERR_INVALID_ARG, "mla_decode: num_splits=%d < -2", num_splits);
     if (B == 0) return ok();
     if (!q || !o_latent || !seq_lens || (max_seq_len > 0 && (!kv_cache || !block_table)))
         return fail(MLA_ERR_INVALID_ARG, "mla_decode: null pointer");
@@ -204,11 +214,14 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: num_blocks=%lld too large (max %d)", (long long)num_blocks,
                     INT32_MAX / mla::kPage);
     int S = mla_resolve_num_splits(num_splits, B, Sq, H, max_seq_len);
-    if (S < 1) return fail(MLA_ERR_CUDA, "mla_decode: could not resolve num_splits (no CUDA device?)");
+    const bool planned = S == -2;
+    if (S < 1 && !planned) return fail(MLA_ERR_CUDA, "mla_decode: could not resolve num_splits (no CUDA device?)");
     if ((int64_t)B * Sq * H > (int64_t)INT32_MAX)
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: B*Sq*H=%lld too large", (long long)B * Sq * H);
-    if ((int64_t)B * Sq * S > (int64_t)1 << 30)
-        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: B*Sq*num_splits=%lld too large", (long long)B * Sq * S);
+    const int pairs = planned ? std::max(1, device_sm_count() / 2) : 1;
+    const int64_t max_units = planned ? mla::plan_max_units((int64_t)B * Sq, pairs) : (int64_t)B * Sq * S;
+    if (max_units > (int64_t)1 << 30)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: %lld work units too many", (long long)max_units);
     const mla::WorkspaceLayout wl = mla::workspace_layout(kv_dtype, B, Sq, H, S, max_seq_len);
     const size_t need = wl.total;
     if (need > 0 && (workspace == nullptr || workspace_bytes < need))
@@ -232,10 +245,17 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
     a.Sq = Sq;
     a.H = H;
     a.scale = scale;
-    a.num_splits = S;
-    if (S > 1) {
+    a.num_splits = planned ? 1 : S;
+    if (wl.partial_slots > 0) {
         a.part_o = (float*)((char*)workspace + wl.part_o);
         a.part_lse = (float*)((char*)workspace + wl.part_lse);
+    }
+    if (planned) {
+        char* base = (char*)workspace + wl.plan;
+        a.plan_count = (const int*)base;
+        a.plan_units = (const int4*)(base + 256);
+        a.plan_rows = (const int2*)(base + (256 + (size_t)max_units * sizeof(int4) + 255) / 256 * 256);
+        a.plan_max_units = (int)max_units;
     }
     const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3_SCALED && max_seq_len > 0;
     if (fp8) {
@@ -253,9 +273,13 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
         e = mla::launch_fp8_expand(a, st);
         if (e != cudaSuccess) return cuda_fail(e, "mla_decode FP8 expand launch");
     }
+    if (planned) {
+        e = mla::launch_plan(a, pairs, st);
+        if (e != cudaSuccess) return cuda_fail(e, "mla_decode schedule launch");
+    }
     e = mla::launch_decode_sm103(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
-    if (S > 1) {
+    if (planned || S > 1) {
         e = mla::launch_merge(a, st);
         if (e != cudaSuccess) return cuda_fail(e, "mla_decode merge launch");
     }

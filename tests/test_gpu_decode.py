@@ -14,7 +14,7 @@ def _oracle(c, sel=None):
                                   c["seq_lens"], c["B"], c["Sq"], c["H"], c["scale"], sel=sel)
 
 
-@pytest.mark.parametrize("num_splits", [1, 2, 3, 0, -1])
+@pytest.mark.parametrize("num_splits", [1, 2, 3, 0, -1, -2])
 def test_tiny_workload(num_splits):
     c = mi.workload_case("tiny")
     o, lse, st = run_decode(c, num_splits)
@@ -23,7 +23,7 @@ def test_tiny_workload(num_splits):
     compare_decode(o, lse, o_ref, lse_ref)
 
 
-@pytest.mark.parametrize("num_splits", [1, 4, 7, 0])
+@pytest.mark.parametrize("num_splits", [1, 4, 7, 0, -2])
 def test_ragged_multi_page(num_splits):
     """Several pages, ragged tails (1, 63, 64, 65 tokens...), poisoned unused rows."""
     c = mi.decode_case(6, 1, 128, [1, 63, 64, 65, 700, 1000], seed=20)
@@ -42,7 +42,7 @@ def test_head_counts(H):
     compare_decode(o, lse, o_ref, lse_ref)
 
 
-@pytest.mark.parametrize("num_splits", [1, 3])
+@pytest.mark.parametrize("num_splits", [1, 3, -2])
 def test_causal_two_row_queries_and_empty_rows(num_splits):
     """Sq = 2: row t sees seq_len - (1 - t) tokens; seq_len 0 and 1 give empty rows."""
     c = mi.decode_case(4, 2, 32, [0, 1, 2, 200], seed=22)
@@ -98,7 +98,7 @@ def _fp8_case(B, Sq, H, lens, seed, vscale=2.0):
     return dict(c, cache=cache.reshape(c["num_blocks"], -1))
 
 
-@pytest.mark.parametrize("num_splits", [1, 3, -1])
+@pytest.mark.parametrize("num_splits", [1, 3, -1, -2])
 def test_fp8_ragged_multi_page(num_splits):
     c = _fp8_case(5, 1, 128, [1, 63, 65, 700, 1000], seed=26)
     o, lse, st = run_decode(c, num_splits)
@@ -133,8 +133,9 @@ def _sampled(c, heads=(0, 37, 127)):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,num_splits", [("dsv3", -1), ("dsv3", 0), ("ragged", -1), ("long_mtp", 0),
-                                             ("long_mtp", -1), ("fp8", -1), ("fp8", 0)])
+@pytest.mark.parametrize("name,num_splits", [("dsv3", -1), ("dsv3", 0), ("dsv3", -2), ("ragged", -1),
+                                             ("ragged", -2), ("long_mtp", 0), ("long_mtp", -1), ("long_mtp", -2),
+                                             ("fp8", -1), ("fp8", 0), ("fp8", -2)])
 def test_full_workload_sampled(name, num_splits):
     c = mi.workload_case(name)
     o, lse, st = run_decode(c, num_splits)
@@ -147,3 +148,27 @@ def test_full_workload_sampled(name, num_splits):
     n = np.array([[oracle.row_len(int(s), c["Sq"], t) for t in range(c["Sq"])] for s in c["seq_lens"]])
     assert np.isfinite(o).all()
     assert np.array_equal(np.isfinite(lse), np.broadcast_to((n > 0)[..., None], lse.shape))
+
+
+def test_batch_invariance_without_splits():
+    """num_splits = 1: a request's output bits do not depend on the batch it is decoded in (its
+    position, its neighbours, the batch size)."""
+    c = mi.decode_case(5, 1, 128, [1000, 37, 4096, 64, 900], seed=29)
+    o_all, lse_all, st = run_decode(c, 1)
+    assert st == 0
+    for b in (0, 2):
+        sub = dict(c, B=1, q=c["q"][b:b + 1], block_table=c["block_table"][b:b + 1], seq_lens=[c["seq_lens"][b]])
+        o1, lse1, st1 = run_decode(sub, 1)
+        assert st1 == 0
+        np.testing.assert_array_equal(o1[0], o_all[b])
+        np.testing.assert_array_equal(lse1[0], lse_all[b])
+
+
+def test_device_schedule_bf16_output_and_one_long_row():
+    """num_splits = -2 with a batch dominated by one long row: that row is cut into several
+    units (partials + merge) while the short rows write their output directly; bf16 output."""
+    c = mi.decode_case(6, 1, 128, [20000, 5, 64, 65, 300, 1], seed=31)
+    o, lse, st = run_decode(c, -2, o_dtype=1)
+    o_ref, lse_ref = _oracle(c)
+    assert st == 0
+    compare_decode(o, lse, o_ref, lse_ref, extra_abs=float(np.abs(o_ref).max()) * 2.0 ** -9)
