@@ -69,6 +69,8 @@ def _load():
                                                   i32, i32, dbl, vp, i64, vp, vp, vp]
         lib.oracle_default_num_splits.restype = i32
         lib.oracle_default_num_splits.argtypes = [i32, i32]
+        lib.oracle_decode_varlen.restype = i32
+        lib.oracle_decode_varlen.argtypes = [vp, vp, i32, i64, vp, i32, vp, vp, i32, i32, dbl, vp, vp]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         lib.oracle_cache_write.restype = i64
@@ -235,3 +237,25 @@ def cache_write(kv_c, k_pe, slot_mapping, kv_dtype, cache, num_blocks, kv_scale=
     return int(_load().oracle_cache_write(kv_c.ctypes.data, kv_c.strides[0] // 2 if T else 0, k_pe.ctypes.data,
                                          k_pe.strides[0] // 2 if T else 0, slots.ctypes.data, T, kv_dtype,
                                          float(kv_scale), cache.ctypes.data, num_blocks))
+
+
+def decode_varlen(q, cache, kv_dtype, num_blocks, block_table, seq_lens, query_start_loc, H, scale):
+    """Route A over packed variable-length query rows: q fp64 or bf16 bits [total_q, H, 576],
+    query_start_loc [B + 1]. Returns (o_latent [total_q, H, 512], lse [total_q, H])."""
+    qsl = np.ascontiguousarray(query_start_loc, np.int32)
+    B = qsl.shape[0] - 1
+    q = np.asarray(q)
+    if q.dtype != np.float64:
+        q = widen_bf16(q)
+    total_q = int(qsl[-1])
+    q = np.ascontiguousarray(q).reshape(total_q, H, D)
+    cache = np.ascontiguousarray(np.asarray(cache).view(np.uint8))
+    bt = np.ascontiguousarray(block_table, np.int32)
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    o = np.empty((total_q, H, L), np.float64)
+    lse = np.empty((total_q, H), np.float64)
+    rc = _load().oracle_decode_varlen(_ptr(q), _ptr(cache), kv_dtype, int(num_blocks), _ptr(bt), bt.shape[1],
+                                      _ptr(sl), _ptr(qsl), B, H, float(scale), _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle: block id out of range")
+    return o, lse

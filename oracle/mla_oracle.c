@@ -528,3 +528,34 @@ int64_t oracle_cache_write(const uint16_t* kv_c, int64_t st_c, const uint16_t* k
     }
     return bad;
 }
+
+/* ------------------------------------------------------------------------------------------
+ * Variable-length query rows ([vLLM-MLA, metadata section]: the VARLEN query-length support
+ * lets a speculative-decoding verification batch mix requests with 1, 2, 3 ... query tokens).
+ * Query rows are packed request after request: request b owns rows
+ * [query_start_loc[b], query_start_loc[b + 1]), and its row t sees
+ * seq_lens[b] - (q_len_b - 1 - t) tokens (clamped at 0), as a uniform batch with Sq = q_len_b.
+ * q is [total_q, H, 576]; o_latent [total_q, H, 512]; lse [total_q, H].
+ * ---------------------------------------------------------------------------------------- */
+int oracle_decode_varlen(const double* q, const uint8_t* cache, int kv_dtype, int64_t num_blocks,
+                         const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                         const int32_t* query_start_loc, int B, int H, double scale,
+                         double* o_latent, double* lse)
+{
+    orc_cache c = {cache, kv_dtype, num_blocks};
+    const int64_t total_q = query_start_loc[B];
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t i = 0; i < total_q * H; ++i) {
+        const int64_t r = i / H, h = i % H;
+        int b = 0;
+        while (b < B && query_start_loc[b + 1] <= r)
+            ++b;
+        const int q_len = query_start_loc[b + 1] - query_start_loc[b];
+        const int t = (int)(r - query_start_loc[b]);
+        const int32_t* bt = block_table + (int64_t)b * max_blocks;
+        const int64_t n = oracle_row_len(seq_lens[b], q_len, t);
+        bad |= oracle_attend_range(q + (r * H + h) * ORC_D, &c, bt, 0, n, scale, o_latent + i * ORC_L, &lse[i]) != 0;
+    }
+    return bad ? -1 : 0;
+}

@@ -413,3 +413,37 @@ def test_cache_write_fp8_quantises_per_definition(kv_scale):
         err = np.abs(deq[inside] / float(ks) - q[inside])
         assert np.all(err <= np.maximum(np.abs(q[inside]) * 2.0 ** -4, 2.0 ** -10) + 1e-12)
         assert np.all(np.abs(deq[~inside] / float(ks)) == 448.0)
+
+
+# ----------------------------------------------------------------------------- variable-length query rows
+def test_varlen_equals_uniform_and_per_request_runs():
+    """Packed rows with equal query lengths are the uniform batch; a request's rows in a mixed
+    batch are that request decoded alone with Sq = its query length."""
+    H = 4
+    c = mi.decode_case(3, 2, H, [5, 130, 70], seed=90)
+    qsl = np.array([0, 2, 4, 6], np.int32)
+    o_u, lse_u = oracle.decode_absorbed(c["q"], c["cache"], c["kv"], c["num_blocks"], c["block_table"],
+                                        c["seq_lens"], 3, 2, H, c["scale"])
+    o_v, lse_v = oracle.decode_varlen(c["q"].reshape(6, H, 576), c["cache"], c["kv"], c["num_blocks"],
+                                      c["block_table"], c["seq_lens"], qsl, H, c["scale"])
+    np.testing.assert_array_equal(o_v, o_u.reshape(6, H, 512))
+    np.testing.assert_array_equal(lse_v, lse_u.reshape(6, H))
+    # mixed query lengths 1, 3, 0, 2 (a request may have no query rows)
+    lens = [40, 200, 9, 64]
+    qlens = [1, 3, 0, 2]
+    d = mi.decode_case(4, 1, H, lens, seed=91)
+    qsl = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    rng = np.random.default_rng(92)
+    q = mi.to_bf16_bits(rng.standard_normal((int(qsl[-1]), H, 576)).astype(np.float32))
+    o_v, lse_v = oracle.decode_varlen(q, d["cache"], d["kv"], d["num_blocks"], d["block_table"], lens, qsl, H,
+                                      d["scale"])
+    for b in range(4):
+        if qlens[b] == 0:
+            continue
+        qb = q[qsl[b]:qsl[b + 1]].reshape(1, qlens[b], H, 576)
+        o_b, lse_b = oracle.decode_absorbed(qb, d["cache"], d["kv"], d["num_blocks"], d["block_table"][b:b + 1],
+                                            [lens[b]], 1, qlens[b], H, d["scale"])
+        np.testing.assert_array_equal(o_v[qsl[b]:qsl[b + 1]], o_b[0])
+        np.testing.assert_array_equal(lse_v[qsl[b]:qsl[b + 1]], lse_b[0])
+    # causal: the last row of request 1 sees all 200 tokens, its first row 198
+    assert np.isfinite(lse_v).all()
