@@ -182,6 +182,24 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
                       float* lse, int32_t* dev_status, mla_stream_t stream);
 
 /*
+ * mla_decode over packed query rows of varying length per request ([vLLM-MLA, metadata section]:
+ * VARLEN query-length support, a speculative-decoding verification batch mixing requests with
+ * 1, 2, 3 ... query tokens). Request b owns query rows [query_start_loc[b], query_start_loc[b+1])
+ * (int32 [B + 1] in device memory, non-decreasing, query_start_loc[0] == 0,
+ * query_start_loc[B] == total_q); its row t sees n = max(0, seq_lens[b] - (q_len_b - 1 - t))
+ * tokens. q is bf16 [total_q, H, 576], o_latent [total_q, H, 512], lse fp32 [total_q, H]; all
+ * other arguments and results as mla_decode, with the workspace from
+ * mla_decode_varlen_workspace_bytes. A request may have no query rows.
+ */
+size_t mla_decode_varlen_workspace_bytes(mla_kv_dtype kv_dtype, int B, int total_q, int H, int num_splits,
+                                         int max_seq_len);
+mla_status mla_decode_varlen(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype, int64_t num_blocks,
+                             const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                             const int32_t* query_start_loc, int max_seq_len, int B, int total_q, int H,
+                             float scale, int num_splits, void* workspace, size_t workspace_bytes, void* o_latent,
+                             mla_dtype o_dtype, float* lse, int32_t* dev_status, mla_stream_t stream);
+
+/*
  * Output up-projection ([vLLM-MLA, two-algorithms section], _v_up_proj: per-head batched GEMM,
  * written token-major):
  *     o[t, h, v] = sum_l o_latent[t, h, l] * W_UV[h, l, v]      (512 -> 128, fp32 accumulate)

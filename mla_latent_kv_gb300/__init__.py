@@ -67,6 +67,11 @@ def lib() -> ctypes.CDLL:
         l.mla_decode_noalloc.restype = i32
         l.mla_decode_noalloc.argtypes = [vp, vp, i32, i64, vp, i32, vp, i32, i32, i32, i32, f32, i32, vp, i32,
                                          vp, vp, vp]
+        l.mla_decode_varlen_workspace_bytes.restype = sz
+        l.mla_decode_varlen_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+        l.mla_decode_varlen.restype = i32
+        l.mla_decode_varlen.argtypes = [vp, vp, i32, i64, vp, i32, vp, vp, i32, i32, i32, i32, f32, i32, vp, sz,
+                                        vp, i32, vp, vp, vp]
         l.mla_cache_write.restype = i32
         l.mla_cache_write.argtypes = [vp, i64, vp, i64, vp, i32, vp, i32, i64, f32, vp, vp]
         l.mla_out_proj.restype = i32
@@ -188,6 +193,34 @@ def decode_noalloc(q, kv_cache, block_table, seq_lens, max_seq_len, scale, kv_dt
                                     block_table.shape[1], _p(seq_lens), int(max_seq_len), B, Sq, H, float(scale),
                                     int(num_splits), _p(o_latent), o_dtype, _p(lse), _p(dev_status),
                                     _stream(stream)))
+    return o_latent, lse
+
+
+def decode_varlen(q, kv_cache, block_table, seq_lens, query_start_loc, max_seq_len, scale, kv_dtype=KV_BF16,
+                  num_splits=0, workspace=None, o_latent=None, o_dtype=DT_F32, lse=None, dev_status=None, stream=None,
+                  num_blocks=None):
+    """q [total_q, H, 576] bf16 packed by query_start_loc [B + 1] int32 (device) ->
+    (o_latent [total_q, H, 512], lse [total_q, H])."""
+    import torch
+    total_q, H = q.shape[0], q.shape[1]
+    B = int(query_start_loc.shape[0]) - 1
+    dev = q.device
+    if num_blocks is None:
+        num_blocks = kv_cache.numel() * kv_cache.element_size() // (PAGE * row_bytes(kv_dtype))
+    S = resolve_num_splits(num_splits, max(total_q, 1), 1, H, max_seq_len)
+    need = int(lib().mla_decode_varlen_workspace_bytes(kv_dtype, B, total_q, H, S, max_seq_len))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if o_latent is None:
+        o_latent = torch.empty((total_q, H, L), dtype=torch.float32 if o_dtype == DT_F32 else torch.bfloat16,
+                               device=dev)
+    if lse is None:
+        lse = torch.empty((total_q, H), dtype=torch.float32, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().mla_decode_varlen(_p(q), _p(kv_cache), kv_dtype, int(num_blocks), _p(block_table),
+                                   block_table.shape[1], _p(seq_lens), _p(query_start_loc), int(max_seq_len), B,
+                                   total_q, H, float(scale), int(S), _p(workspace), ws_bytes, _p(o_latent), o_dtype,
+                                   _p(lse), _p(dev_status), _stream(stream)))
     return o_latent, lse
 
 

@@ -145,8 +145,8 @@ __device__ __forceinline__ RowGeom row_geometry(const DecodeArgs& p, int unit, b
         split_range(visible_tokens(p, g.r, report), S, unit % S, &g.j0, &g.j1);
         g.slot = S > 1 ? unit : -1;
     }
-    g.b = g.r / p.Sq;
-    g.t = g.r % p.Sq;
+    int q_len;
+    row_request(p, g.r, &g.b, &g.t, &q_len);
     g.npages = (g.j1 - g.j0 + kPage - 1) / kPage;
     g.page0 = g.j0 / kPage;
     return g;
@@ -746,13 +746,13 @@ cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s) {
     memset(&o_map, 0, sizeof o_map);
     memset(&p_map, 0, sizeof p_map);
     const bool planned = a.plan_units != nullptr;
-    const int64_t units = planned ? a.plan_max_units : (int64_t)a.B * a.Sq * a.num_splits;
+    const int64_t units = planned ? a.plan_max_units : (int64_t)a.rows * a.num_splits;
     {
         // final rows [row][head][512] of o_latent; one box is one 128-byte-wide column panel
         // of one row's H heads
         const bool f32 = a.o_dtype == MLA_DT_F32;
         const uint64_t es = f32 ? 4 : 2;
-        const uint64_t dims[3] = {(uint64_t)kL, (uint64_t)a.H, (uint64_t)a.B * a.Sq};
+        const uint64_t dims[3] = {(uint64_t)kL, (uint64_t)a.H, (uint64_t)a.rows};
         const uint64_t strides[2] = {(uint64_t)kL * es, (uint64_t)a.H * kL * es};
         const uint32_t box[3] = {(uint32_t)(128 / es), (uint32_t)a.H, 1u};
         e = encode_tmap(&o_map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
@@ -776,7 +776,7 @@ cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s) {
         e = encode_tmap(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, fp8 ? (const void*)a.fp8_rows : a.cache, dims,
                         strides, box, true);
         if (e != cudaSuccess) return e;
-        const uint64_t qdims[2] = {(uint64_t)kD, (uint64_t)a.B * a.Sq * a.H};
+        const uint64_t qdims[2] = {(uint64_t)kD, (uint64_t)a.rows * a.H};
         const uint32_t qbox[2] = {64, 128};
         e = encode_tmap(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, qdims, strides, qbox, true);
         if (e != cudaSuccess) return e;

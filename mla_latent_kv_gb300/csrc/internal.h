@@ -27,7 +27,9 @@ struct DecodeArgs {
     int max_blocks;
     const int32_t* seq_lens;    // [B]
     int max_seq_len;
-    int B, Sq, H;
+    int B, Sq, H;               // requests, uniform query rows per request (1 for packed rows), heads
+    int rows;                   // query rows: B * Sq, or the packed total
+    const int32_t* qsl;         // packed rows: request b owns rows [qsl[b], qsl[b + 1]); else null
     float scale;
     int num_splits;             // resolved, >= 1
     float* part_o;              // [B*Sq, S, H, 512] fp32 (num_splits > 1)
@@ -49,18 +51,41 @@ struct DecodeArgs {
     int plan_max_units;         // the grid is sized for this many units
 };
 
-// Visible tokens of query row r (request r / Sq, position r % Sq): seq_len - (Sq - 1 - t),
-// clamped at 0, with seq_len clamped to what the block table (or the FP8 expansion) can hold;
-// an out-of-range seq_len sets MLA_DEV_SEQ_TOO_LONG when `report`.
+// Request b, position t and query length of query row r: uniform rows are r = b * Sq + t;
+// packed rows belong to the last request whose first row is <= r (binary search of qsl).
+__device__ __forceinline__ void row_request(const DecodeArgs& p, int r, int* b, int* t, int* q_len) {
+    if (p.qsl == nullptr) {
+        *b = r / p.Sq;
+        *t = r % p.Sq;
+        *q_len = p.Sq;
+        return;
+    }
+    int lo = 0, hi = p.B - 1;  // invariant: qsl[lo] <= r
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.qsl[mid] <= r)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    *b = lo;
+    *t = r - p.qsl[lo];
+    *q_len = p.qsl[lo + 1] - p.qsl[lo];
+}
+
+// Visible tokens of query row r: seq_len - (q_len - 1 - t), clamped at 0, with seq_len clamped
+// to what the block table (or the FP8 expansion) can hold; an out-of-range seq_len sets
+// MLA_DEV_SEQ_TOO_LONG when `report`.
 __device__ __forceinline__ int visible_tokens(const DecodeArgs& p, int r, bool report) {
-    const int b = r / p.Sq, t = r % p.Sq;
+    int b, t, q_len;
+    row_request(p, r, &b, &t, &q_len);
     int seq = p.seq_lens[b];
     const int cap = (p.fp8_mp > 0 && p.fp8_mp < p.max_blocks ? p.fp8_mp : p.max_blocks) * MLA_PAGE_SIZE;
     if (seq > cap || seq > p.max_seq_len || seq < 0) {
         if (report && p.dev_status) atomicOr(p.dev_status, MLA_DEV_SEQ_TOO_LONG);
         seq = seq < 0 ? 0 : (seq > cap ? cap : seq);
     }
-    const int n = seq - (p.Sq - 1 - t);
+    const int n = seq - (q_len - 1 - t);
     return n < 0 ? 0 : n;
 }
 
@@ -73,7 +98,8 @@ struct WorkspaceLayout {
     size_t plan, part_o, part_lse, fp8_rows, fp8_scales, total;
     int64_t partial_slots;  // rows of part_o / part_lse
 };
-WorkspaceLayout workspace_layout(int kv_dtype, int B, int Sq, int H, int num_splits, int max_seq_len);
+// B requests (the FP8 expansion is per request) and `rows` query rows (split partials per row).
+WorkspaceLayout workspace_layout(int kv_dtype, int B, int64_t rows, int H, int num_splits, int max_seq_len);
 
 // Token range [j0, j1) of split s of a row with n visible tokens: the row is cut into
 // num_splits page-aligned chunks of round_up(ceil(n / S), 64) tokens; trailing splits may be

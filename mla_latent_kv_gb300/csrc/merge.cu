@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(DecodeArgs p) {
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();  // the partials are the preceding kernel's output
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int64_t n_items = (int64_t)p.B * p.Sq * p.H;
+    const int64_t n_items = (int64_t)p.rows * p.H;
     // grid-stride over (row, head); with a device-built schedule most rows have no partials
     // and their items are skipped after one load
     for (int64_t item = (int64_t)blockIdx.x * kWarps + warp; item < n_items; item += (int64_t)gridDim.x * kWarps) {
@@ -94,7 +94,7 @@ __device__ __forceinline__ void merge_item(const DecodeArgs& p, int64_t r, int h
 }  // namespace
 
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
-    const int64_t n_items = (int64_t)a.B * a.Sq * a.H;
+    const int64_t n_items = (int64_t)a.rows * a.H;
     int64_t blocks = (n_items + kWarps - 1) / kWarps;
     if (a.plan_rows && blocks > 1216) blocks = 1216;  // grid-stride; the split rows are few
     return launch_pdl(merge_kernel, dim3((unsigned)blocks), dim3(kWarps * 32), 0, s, a);

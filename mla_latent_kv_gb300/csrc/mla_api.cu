@@ -48,18 +48,18 @@ int device_sm_count() {
 }  // namespace
 
 namespace mla {
-WorkspaceLayout workspace_layout(int kv_dtype, int B, int Sq, int H, int num_splits, int max_seq_len) {
+WorkspaceLayout workspace_layout(int kv_dtype, int B, int64_t rows, int H, int num_splits, int max_seq_len) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     WorkspaceLayout w{};
-    if (B <= 0 || Sq <= 0 || H <= 0) return w;
+    if (B <= 0 || rows <= 0 || H <= 0) return w;
     size_t off = 0;
-    int64_t slots = num_splits > 1 ? (int64_t)B * Sq * num_splits : 0;
+    int64_t slots = num_splits > 1 ? rows * num_splits : 0;
     if (num_splits == -2) {  // device-built schedule: header, unit list, per-row slots
         const int sms = device_sm_count();
         if (sms < 1) return w;
-        slots = plan_max_units((int64_t)B * Sq, sms / 2 > 0 ? sms / 2 : 1);
+        slots = plan_max_units(rows, sms / 2 > 0 ? sms / 2 : 1);
         w.plan = 0;
-        off = up(256 + (size_t)slots * sizeof(int4)) + up((size_t)B * Sq * sizeof(int2));
+        off = up(256 + (size_t)slots * sizeof(int4)) + up((size_t)rows * sizeof(int2));
     }
     if (slots > 0) {
         const size_t units = (size_t)slots * H;
@@ -152,12 +152,20 @@ int mla_resolve_num_splits(int num_splits, int B, int Sq, int H, int max_seq_len
 }
 
 size_t mla_decode_workspace_bytes(int B, int Sq, int H, int num_splits) {
-    return mla::workspace_layout(MLA_KV_BF16, B, Sq, H, num_splits, 0).total;
+    if (Sq <= 0) return 0;
+    return mla::workspace_layout(MLA_KV_BF16, B, (int64_t)B * Sq, H, num_splits, 0).total;
 }
 
 size_t mla_decode_workspace_bytes_kv(mla_kv_dtype kv_dtype, int B, int Sq, int H, int num_splits, int max_seq_len) {
     if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3_SCALED) return 0;
-    return mla::workspace_layout(kv_dtype, B, Sq, H, num_splits, max_seq_len).total;
+    if (Sq <= 0) return 0;
+    return mla::workspace_layout(kv_dtype, B, (int64_t)B * Sq, H, num_splits, max_seq_len).total;
+}
+
+size_t mla_decode_varlen_workspace_bytes(mla_kv_dtype kv_dtype, int B, int total_q, int H, int num_splits,
+                                         int max_seq_len) {
+    if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3_SCALED) return 0;
+    return mla::workspace_layout(kv_dtype, B, total_q, H, num_splits, max_seq_len).total;
 }
 
 mla_status mla_absorb_q(const void* q_nope, int64_t snt, int64_t snh, const void* q_pe, int64_t spt,
@@ -182,13 +190,17 @@ mla_status mla_absorb_q(const void* q_nope, int64_t snt, int64_t snh, const void
     return ok();
 }
 
-mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype, int64_t num_blocks,
-                      const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int max_seq_len,
-                      int B, int Sq, int H, float scale, int num_splits, void* workspace,
-                      size_t workspace_bytes, void* o_latent, mla_dtype o_dtype, float* lse,
-                      int32_t* dev_status, mla_stream_t stream) {
-    if (B < 0) return fail(MLA_ERR_INVALID_ARG, "mla_decode: B=%d < 0", B);
-    if (Sq < 1) return fail(MLA_ERR_INVALID_ARG, "mla_decode: Sq=%d < 1", Sq);
+}  // extern "C"
+
+namespace {
+
+// Shared body of mla_decode (uniform Sq rows per request, qsl == nullptr) and mla_decode_varlen
+// (packed rows, qsl = query_start_loc, Sq == 1): `rows` query rows of q / o_latent / lse.
+mla_status decode_impl(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype, int64_t num_blocks,
+                       const int32_t* block_table, int max_blocks, const int32_t* seq_lens, const int32_t* qsl,
+                       int max_seq_len, int B, int Sq, int64_t rows, int H, float scale, int num_splits,
+                       void* workspace, size_t workspace_bytes, void* o_latent, mla_dtype o_dtype, float* lse,
+                       int32_t* dev_status, mla_stream_t stream) {
     if (H < 1 || H > MLA_MAX_HEADS)
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: H=%d outside [1, %d]", H, MLA_MAX_HEADS);
     if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3_SCALED)
@@ -203,9 +215,10 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
     if (!(std::isfinite(scale)) || scale <= 0.f)
         return fail(MLA_ERR_INVALID_ARG, "mla_decode: scale must be finite and > 0");
     if (num_splits < -2) return fail(MLA_ERR_INVALID_ARG, "mla_decode: num_splits=%d < -2", num_splits);
-    if (B == 0) return ok();
+    if (B == 0 || rows == 0) return ok();
     if (!q || !o_latent || !seq_lens || (max_seq_len > 0 && (!kv_cache || !block_table)))
         return fail(MLA_ERR_INVALID_ARG, "mla_decode: null pointer");
+    if (rows > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "mla_decode: %lld query rows too many", (long long)rows);
     if (!aligned16(q) || (kv_cache && !aligned16(kv_cache)) || !aligned16(o_latent))
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: q, kv_cache and o_latent must be 16-byte aligned");
     if (kv_dtype == MLA_KV_FP8_E4M3_SCALED && (max_seq_len + mla::kPage - 1) / mla::kPage > 65535)
@@ -213,16 +226,16 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
     if (num_blocks > (int64_t)(INT32_MAX / mla::kPage))
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: num_blocks=%lld too large (max %d)", (long long)num_blocks,
                     INT32_MAX / mla::kPage);
-    int S = mla_resolve_num_splits(num_splits, B, Sq, H, max_seq_len);
+    int S = mla_resolve_num_splits(num_splits, (int)rows, 1, H, max_seq_len);
     const bool planned = S == -2;
     if (S < 1 && !planned) return fail(MLA_ERR_CUDA, "mla_decode: could not resolve num_splits (no CUDA device?)");
-    if ((int64_t)B * Sq * H > (int64_t)INT32_MAX)
-        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: B*Sq*H=%lld too large", (long long)B * Sq * H);
+    if (rows * H > (int64_t)INT32_MAX)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: rows*H=%lld too large", (long long)(rows * H));
     const int pairs = planned ? std::max(1, device_sm_count() / 2) : 1;
-    const int64_t max_units = planned ? mla::plan_max_units((int64_t)B * Sq, pairs) : (int64_t)B * Sq * S;
+    const int64_t max_units = planned ? mla::plan_max_units(rows, pairs) : rows * S;
     if (max_units > (int64_t)1 << 30)
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: %lld work units too many", (long long)max_units);
-    const mla::WorkspaceLayout wl = mla::workspace_layout(kv_dtype, B, Sq, H, S, max_seq_len);
+    const mla::WorkspaceLayout wl = mla::workspace_layout(kv_dtype, B, rows, H, S, max_seq_len);
     const size_t need = wl.total;
     if (need > 0 && (workspace == nullptr || workspace_bytes < need))
         return fail(MLA_ERR_WORKSPACE_TOO_SMALL,
@@ -243,6 +256,8 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
     a.max_seq_len = max_seq_len;
     a.B = B;
     a.Sq = Sq;
+    a.rows = (int)rows;
+    a.qsl = qsl;
     a.H = H;
     a.scale = scale;
     a.num_splits = planned ? 1 : S;
@@ -284,6 +299,34 @@ mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype
         if (e != cudaSuccess) return cuda_fail(e, "mla_decode merge launch");
     }
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype, int64_t num_blocks,
+                      const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int max_seq_len,
+                      int B, int Sq, int H, float scale, int num_splits, void* workspace,
+                      size_t workspace_bytes, void* o_latent, mla_dtype o_dtype, float* lse,
+                      int32_t* dev_status, mla_stream_t stream) {
+    if (B < 0) return fail(MLA_ERR_INVALID_ARG, "mla_decode: B=%d < 0", B);
+    if (Sq < 1) return fail(MLA_ERR_INVALID_ARG, "mla_decode: Sq=%d < 1", Sq);
+    return decode_impl(q, kv_cache, kv_dtype, num_blocks, block_table, max_blocks, seq_lens, nullptr, max_seq_len,
+                       B, Sq, (int64_t)B * Sq, H, scale, num_splits, workspace, workspace_bytes, o_latent, o_dtype,
+                       lse, dev_status, stream);
+}
+
+mla_status mla_decode_varlen(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype, int64_t num_blocks,
+                             const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                             const int32_t* query_start_loc, int max_seq_len, int B, int total_q, int H,
+                             float scale, int num_splits, void* workspace, size_t workspace_bytes, void* o_latent,
+                             mla_dtype o_dtype, float* lse, int32_t* dev_status, mla_stream_t stream) {
+    if (B < 0 || total_q < 0) return fail(MLA_ERR_INVALID_ARG, "mla_decode_varlen: B=%d, total_q=%d", B, total_q);
+    if (total_q > 0 && !query_start_loc) return fail(MLA_ERR_INVALID_ARG, "mla_decode_varlen: null query_start_loc");
+    return decode_impl(q, kv_cache, kv_dtype, num_blocks, block_table, max_blocks, seq_lens, query_start_loc,
+                       max_seq_len, B, 1, total_q, H, scale, num_splits, workspace, workspace_bytes, o_latent,
+                       o_dtype, lse, dev_status, stream);
 }
 
 mla_status mla_cache_write(const void* kv_c, int64_t kv_c_stride_t, const void* k_pe, int64_t k_pe_stride_t,

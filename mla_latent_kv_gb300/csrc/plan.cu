@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(DecodeArgs p, int pairs)
     __shared__ int s_cand[kCands];
     __shared__ float s_cost[kCands];
     __shared__ int s_best;
-    const int R = p.B * p.Sq;
+    const int R = p.rows;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per = (R + kThreads - 1) / kThreads;
     const int r0 = min(R, tid * per), r1 = min(R, r0 + per);

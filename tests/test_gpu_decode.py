@@ -172,3 +172,41 @@ def test_device_schedule_bf16_output_and_one_long_row():
     o_ref, lse_ref = _oracle(c)
     assert st == 0
     compare_decode(o, lse, o_ref, lse_ref, extra_abs=float(np.abs(o_ref).max()) * 2.0 ** -9)
+
+
+# ----------------------------------------------------------------------------- packed variable-length rows
+def _varlen_case(lens, qlens, H, seed, kv=mi.KV_BF16):
+    c = mi.decode_case(len(lens), 1, H, lens, kv=kv, seed=seed)
+    qsl = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    rng = np.random.default_rng(seed + 1)
+    q = mi.to_bf16_bits(rng.standard_normal((int(qsl[-1]), H, 576)).astype(np.float32))
+    return dict(c, q=q, qsl=qsl)
+
+
+@pytest.mark.parametrize("num_splits", [1, 3, -1, -2])
+@pytest.mark.parametrize("kv", [mi.KV_BF16, mi.KV_FP8])
+def test_varlen_mixed_query_lengths(num_splits, kv):
+    import torch
+    import mla_latent_kv_gb300 as mla
+    v = _varlen_case([40, 700, 9, 64, 3000, 2], [1, 3, 0, 2, 4, 2], 64, seed=33, kv=kv)
+    d = torch_dev(v)
+    qsl = torch.from_numpy(v["qsl"]).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, lse = mla.decode_varlen(d["q"], d["cache"], d["block_table"], d["seq_lens"], qsl, max(v["seq_lens"]),
+                               v["scale"], kv_dtype=kv, num_splits=num_splits, dev_status=st,
+                               num_blocks=v["num_blocks"])
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    o_ref, lse_ref = oracle.decode_varlen(v["q"], v["cache"], kv, v["num_blocks"], v["block_table"], v["seq_lens"],
+                                          v["qsl"], 64, v["scale"])
+    from parity_util import to_f64
+    compare_decode(to_f64(o), to_f64(lse), o_ref, lse_ref, fp8=kv == mi.KV_FP8)
+
+
+def test_uniform_four_token_queries():
+    """Sq > 2 through the uniform entry point (MTP-style rows sharing one request's cache)."""
+    c = mi.decode_case(3, 4, 32, [3, 500, 129], seed=34)
+    o, lse, st = run_decode(c, -1)
+    o_ref, lse_ref = _oracle(c)
+    assert st == 0
+    compare_decode(o, lse, o_ref, lse_ref)
