@@ -186,3 +186,30 @@ def out_proj_case(T, H, seed=0):
     rng = np.random.default_rng(seed)
     return dict(T=T, H=H, o_latent=rng.standard_normal((T, H, L), dtype=np.float32),
                 w_uv=normal_bf16(rng, (H, L, V), std=1.0 / math.sqrt(512.0)))
+
+
+def prefill_case(ctx_lens, q_lens, H, kv=KV_BF16, seed=0, spare_blocks=4, poison=True):
+    """Inputs of the prefill route: request b has ctx_lens[b] tokens in the paged cache and q_lens[b]
+    new tokens, packed by query_start_loc. The block table already covers the new tokens'
+    positions (their cache rows are poisoned here; a test that needs them writes them). Returns a
+    dict: q [T, H, 192] (q_nope || q_pe), kv_c_new [T, 512], k_pe_new [T, 64] (bf16 bits),
+    W_UK_T [H, 128, 512], W_UV [H, 512, 128] (N(0, 1/512)), new_slots [T] int64 (cache slot of
+    each new token), plus the cache and its metadata."""
+    rng = np.random.default_rng(seed)
+    ctx = np.asarray(ctx_lens, np.int32)
+    ql = np.asarray(q_lens, np.int32)
+    qsl = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    bt, num_blocks = make_block_table(ctx.astype(np.int64) + ql, rng, spare_blocks)
+    valid = valid_row_mask(ctx, bt, num_blocks) if poison else None
+    cache = make_cache(num_blocks, kv, rng, valid, poison)
+    T = int(qsl[-1])
+    slots = np.zeros(T, np.int64)
+    for b in range(len(ctx)):
+        for i in range(int(ql[b])):
+            pos = int(ctx[b]) + i
+            slots[qsl[b] + i] = int(bt[b, pos // PAGE]) * PAGE + pos % PAGE
+    return dict(H=H, kv=kv, ctx_lens=ctx, query_start_loc=qsl, block_table=bt, num_blocks=num_blocks,
+                cache=cache, q=normal_bf16(rng, (T, H, P + R)), kv_c_new=normal_bf16(rng, (T, L)),
+                k_pe_new=normal_bf16(rng, (T, R)), new_slots=slots,
+                w_uk_t=normal_bf16(rng, (H, P, L), std=1.0 / math.sqrt(512.0)),
+                w_uv=normal_bf16(rng, (H, L, V), std=1.0 / math.sqrt(512.0)), scale=SCALE)

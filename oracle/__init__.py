@@ -75,6 +75,11 @@ def _load():
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         lib.oracle_cache_write.restype = i64
         lib.oracle_cache_write.argtypes = [vp, i64, vp, i64, vp, i64, i32, ctypes.c_float, vp, i64]
+        lib.oracle_prefill_chunks.restype = i64
+        lib.oracle_prefill_chunks.argtypes = [vp, i32, i64, vp]
+        lib.oracle_prefill.restype = i32
+        lib.oracle_prefill.argtypes = [vp, vp, vp, vp, i32, i64, vp, i32, vp, vp, i32, i32, vp, vp, dbl, i64,
+                                       vp, vp]
         _lib = lib
         return lib
 
@@ -259,3 +264,43 @@ def decode_varlen(q, cache, kv_dtype, num_blocks, block_table, seq_lens, query_s
     if rc != 0:
         raise ValueError("oracle: block id out of range")
     return o, lse
+
+
+def prefill_chunks(ctx_lens, chunk_rows):
+    """The context chunk plan: int64 [n, 4] rows (chunk, request, first position, tokens)."""
+    cl = np.ascontiguousarray(ctx_lens, np.int32)
+    lib = _load()
+    n = lib.oracle_prefill_chunks(_ptr(cl), cl.shape[0], int(chunk_rows), None)
+    if n < 0:
+        raise ValueError("oracle: chunk_rows must hold at least one page")
+    out = np.zeros((max(n, 1), 4), np.int64)
+    lib.oracle_prefill_chunks(_ptr(cl), cl.shape[0], int(chunk_rows), _ptr(out))
+    return out[:n]
+
+
+def prefill(q, kv_c_new, k_pe_new, cache, kv_dtype, num_blocks, block_table, ctx_lens, query_start_loc, H,
+            w_uk_t, w_uv, scale, chunk_rows):
+    """Prefill (compute-friendly route): q bf16 bits [total_q, H, 192], the new tokens' kv_c
+    [total_q, 512] and k_pe [total_q, 64] (bf16 bits), the context in the paged cache.
+    Returns (o [total_q, H, 128], lse [total_q, H]) in fp64."""
+    qsl = np.ascontiguousarray(query_start_loc, np.int32)
+    B = qsl.shape[0] - 1
+    total_q = int(qsl[-1])
+    qq = _u16(q).reshape(total_q, H, P + R)
+    kc = _u16(kv_c_new).reshape(total_q, L)
+    kp = _u16(k_pe_new).reshape(total_q, R)
+    cache = np.ascontiguousarray(np.asarray(cache).view(np.uint8))
+    bt = np.ascontiguousarray(block_table, np.int32)
+    cl = np.ascontiguousarray(ctx_lens, np.int32)
+    wk = _u16(w_uk_t)
+    wv = _u16(w_uv)
+    o = np.empty((max(total_q, 1), H, V), np.float64)
+    lse = np.empty((max(total_q, 1), H), np.float64)
+    rc = _load().oracle_prefill(_ptr(qq), _ptr(kc), _ptr(kp), _ptr(cache), kv_dtype, int(num_blocks), _ptr(bt),
+                                bt.shape[1], _ptr(cl), _ptr(qsl), B, H, _ptr(wk), _ptr(wv), float(scale),
+                                int(chunk_rows), _ptr(o), _ptr(lse))
+    if rc == -2:
+        raise ValueError("oracle: chunk_rows must hold at least one page")
+    if rc != 0:
+        raise ValueError("oracle: block id out of range")
+    return o[:total_q], lse[:total_q]

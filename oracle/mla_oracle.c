@@ -559,3 +559,271 @@ int oracle_decode_varlen(const double* q, const uint8_t* cache, int kv_dtype, in
     }
     return bad ? -1 : 0;
 }
+
+/* ==========================================================================================
+ * Prefill, the compute-friendly route ([vLLM-MLA, Prefill section]). A prefill request b has
+ * ctx_lens[b] tokens already in the paged cache (its context, positions 0 .. ctx-1) and q_len_b
+ * new tokens (positions ctx .. ctx + q_len - 1), packed request after request by
+ * query_start_loc. Keys and values are up-projected per head (no absorption):
+ *     k_nope_j[p] = sum_l c_j[l] W_UK_T[h, p, l],   k_j = [k_nope_j (128) || k_pe_j (64)]
+ *     v_j[v]      = sum_l c_j[l] W_UV[h, l, v]
+ * and attention is standard MHA with a 192-dim q.k and a 128-dim output. The page's order:
+ *   1. the new tokens attend causally among themselves (new token i is visible to query t of
+ *      the same request iff i <= t); their k/v come from the step's own kv_c / k_pe;
+ *   2. the context is processed in chunks of at most chunk_rows gathered rows: each chunk is
+ *      gathered from the paged cache (FP8 rows dequantised: the K side with k_scale, the V side
+ *      with v_scale), up-projected, and attended by every query of the requests it holds (all
+ *      context tokens precede the new ones, so no mask); the chunk results are accumulated;
+ *   3. the context result (prefix) and the new-token result (suffix) are merged by their lse
+ *      (merge_attn_states); a request without context has an empty prefix (o = 0, lse = -inf).
+ * ======================================================================================== */
+
+/* Merge of two partial states of one (row, head) with n output dims -- the same formula as
+ * oracle_merge, for the prefix / suffix pair:  M = max(lse_a, lse_b), w = exp(lse - M). */
+static void orc_merge_pair(double* o_acc, double* lse_acc, const double* o_new, double lse_new, int n)
+{
+    const double la = *lse_acc;
+    const double M = la > lse_new ? la : lse_new;
+    if (M == -INFINITY)
+        return; /* both empty: o stays 0, lse -inf */
+    const double wa = la == -INFINITY ? 0.0 : exp(la - M);
+    const double wb = lse_new == -INFINITY ? 0.0 : exp(lse_new - M);
+    for (int d = 0; d < n; ++d)
+        o_acc[d] = (wa * o_acc[d] + wb * o_new[d]) / (wa + wb);
+    *lse_acc = M + log(wa + wb);
+}
+
+/* ------------------------------------------------------------------------------------------
+ * Context chunk plan ([vLLM-MLA, Prefill section]: the contexts are packed into chunks of at
+ * most row_budget rows; a request that does not fit is cut, and every chunk starts on a page
+ * boundary of its request). Requests are taken in order; a request's remaining context goes
+ * into the open chunk whole if it fits, otherwise as many whole pages as still fit, and a chunk
+ * with no room for a page is closed. Each emitted piece is (chunk, request, first position,
+ * token count); pieces of one chunk are consecutive. chunk_rows < 64 is rejected (-1), as no
+ * page would fit. Returns the number of pieces (pieces may be NULL to count them).
+ * ---------------------------------------------------------------------------------------- */
+int64_t oracle_prefill_chunks(const int32_t* ctx_lens, int B, int64_t chunk_rows, int64_t* pieces)
+{
+    if (chunk_rows < ORC_PAGE)
+        return -1;
+    int64_t n = 0, chunk = 0, used = 0;
+    for (int b = 0; b < B; ++b) {
+        int64_t pos = 0;
+        const int64_t len = ctx_lens[b] > 0 ? ctx_lens[b] : 0;
+        while (pos < len) {
+            int64_t take = len - pos;
+            if (take > chunk_rows - used) {
+                take = (chunk_rows - used) / ORC_PAGE * ORC_PAGE;
+                if (take == 0) { /* no whole page fits: close the chunk */
+                    ++chunk;
+                    used = 0;
+                    continue;
+                }
+            }
+            if (pieces) {
+                pieces[4 * n + 0] = chunk;
+                pieces[4 * n + 1] = b;
+                pieces[4 * n + 2] = pos;
+                pieces[4 * n + 3] = take;
+            }
+            ++n;
+            used += take;
+            pos += take;
+        }
+    }
+    return n;
+}
+
+/* Up-projection of one latent row for head h: k_nope (128) from the K-side latent ck, v (128)
+ * from the V-side latent cv (the same values for a bf16 cache). */
+static void orc_up_project(const double* ck, const double* cv, const uint16_t* w_uk_t,
+                           const uint16_t* w_uv, int64_t h, double* k_nope, double* v)
+{
+    for (int p = 0; p < ORC_P; ++p) {
+        double acc = 0.0;
+        for (int l = 0; l < ORC_L; ++l)
+            acc += ck[l] * oracle_bf16_value(w_uk_t[(h * ORC_P + p) * ORC_L + l]);
+        k_nope[p] = acc;
+    }
+    for (int vv = 0; vv < ORC_V; ++vv) {
+        double acc = 0.0;
+        for (int l = 0; l < ORC_L; ++l)
+            acc += cv[l] * oracle_bf16_value(w_uv[(h * ORC_L + l) * ORC_V + vv]);
+        v[vv] = acc;
+    }
+}
+
+/* Standard attention of one query (192 dims: q_nope 128 || q_pe 64) over n keys, each 192 dims
+ * (k_nope || k_pe) with a 128-dim value: two plain passes (logits and their max, then weights
+ * and the weighted sum). n = 0 gives o = 0, lse = -inf. */
+static void orc_mha_row(const double* q, const double* k, const double* v, int64_t n, double scale,
+                        double* o, double* lse)
+{
+    for (int d = 0; d < ORC_V; ++d)
+        o[d] = 0.0;
+    if (n == 0) {
+        *lse = -INFINITY;
+        return;
+    }
+    double* s = (double*)malloc((size_t)n * sizeof(double));
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < ORC_P + ORC_R; ++d)
+            dot += q[d] * k[j * (ORC_P + ORC_R) + d];
+        s[j] = scale * dot;
+        if (s[j] > m)
+            m = s[j];
+    }
+    double sum = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        const double w = exp(s[j] - m);
+        sum += w;
+        for (int d = 0; d < ORC_V; ++d)
+            o[d] += w * v[j * ORC_V + d];
+    }
+    for (int d = 0; d < ORC_V; ++d)
+        o[d] /= sum;
+    *lse = m + log(sum);
+    free(s);
+}
+
+/* ------------------------------------------------------------------------------------------
+ *   q          [total_q, H, 192] bf16 (q_nope || q_pe per head, RoPE already applied)
+ *   kv_c_new   [total_q, 512] bf16, k_pe_new [total_q, 64] bf16: the new tokens' latent rows
+ *   cache      raw bytes [num_blocks, 64, row_bytes] holding each request's context
+ *   ctx_lens   [B], query_start_loc [B + 1] (total_q = query_start_loc[B])
+ *   chunk_rows the context row budget per chunk (>= 64)
+ *   o          [total_q, H, 128], lse [total_q, H]
+ * Returns 0, -1 on a bad block id, -2 on chunk_rows < 64.
+ * ---------------------------------------------------------------------------------------- */
+int oracle_prefill(const uint16_t* q, const uint16_t* kv_c_new, const uint16_t* k_pe_new,
+                   const uint8_t* cache, int kv_dtype, int64_t num_blocks, const int32_t* block_table,
+                   int max_blocks, const int32_t* ctx_lens, const int32_t* query_start_loc, int B, int H,
+                   const uint16_t* w_uk_t, const uint16_t* w_uv, double scale, int64_t chunk_rows,
+                   double* o, double* lse)
+{
+    const int KD = ORC_P + ORC_R; /* 192 */
+    const int64_t total_q = query_start_loc[B];
+    const int64_t n_pieces = oracle_prefill_chunks(ctx_lens, B, chunk_rows, NULL);
+    if (n_pieces < 0)
+        return -2;
+    int64_t* pieces = (int64_t*)malloc((size_t)(n_pieces > 0 ? n_pieces : 1) * 4 * sizeof(int64_t));
+    oracle_prefill_chunks(ctx_lens, B, chunk_rows, pieces);
+    orc_cache c = {cache, kv_dtype, num_blocks};
+
+    /* row r of the packed queries belongs to request req[r] */
+    int* req = (int*)malloc((size_t)(total_q > 0 ? total_q : 1) * sizeof(int));
+    for (int b = 0; b < B; ++b)
+        for (int64_t r = query_start_loc[b]; r < query_start_loc[b + 1]; ++r)
+            req[r] = b;
+
+    /* ---- step 1: the new tokens (suffix) ---- */
+    double* kn = (double*)malloc((size_t)(total_q > 0 ? total_q : 1) * H * KD * sizeof(double));
+    double* vn = (double*)malloc((size_t)(total_q > 0 ? total_q : 1) * H * ORC_V * sizeof(double));
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < total_q * H; ++i) {
+        const int64_t r = i / H, h = i % H;
+        double cl[ORC_L];
+        for (int l = 0; l < ORC_L; ++l)
+            cl[l] = oracle_bf16_value(kv_c_new[r * ORC_L + l]);
+        /* key / value rows stored head-major so that one head's keys are contiguous */
+        double* kk = kn + (h * total_q + r) * KD;
+        orc_up_project(cl, cl, w_uk_t, w_uv, h, kk, vn + (h * total_q + r) * ORC_V);
+        for (int e = 0; e < ORC_R; ++e)
+            kk[ORC_P + e] = oracle_bf16_value(k_pe_new[r * ORC_R + e]);
+    }
+    double* o_suf = (double*)malloc((size_t)(total_q > 0 ? total_q : 1) * H * ORC_V * sizeof(double));
+    double* l_suf = (double*)malloc((size_t)(total_q > 0 ? total_q : 1) * H * sizeof(double));
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < total_q * H; ++i) {
+        const int64_t r = i / H, h = i % H;
+        const int b = req[r];
+        const int64_t first = query_start_loc[b];
+        double qq[ORC_P + ORC_R];
+        for (int d = 0; d < KD; ++d)
+            qq[d] = oracle_bf16_value(q[(r * H + h) * KD + d]);
+        /* causal: new tokens first .. r of the request */
+        orc_mha_row(qq, kn + (h * total_q + first) * KD, vn + (h * total_q + first) * ORC_V,
+                    r - first + 1, scale, o_suf + i * ORC_V, &l_suf[i]);
+    }
+    free(kn);
+    free(vn);
+
+    /* ---- step 2: the context, chunk by chunk (prefix) ---- */
+    for (int64_t i = 0; i < total_q * H; ++i) {
+        for (int d = 0; d < ORC_V; ++d)
+            o[i * ORC_V + d] = 0.0;
+        lse[i] = -INFINITY;
+    }
+    int bad = 0;
+    int64_t p0 = 0;
+    while (p0 < n_pieces) {
+        int64_t p1 = p0;
+        int64_t rows = 0;
+        while (p1 < n_pieces && pieces[4 * p1] == pieces[4 * p0])
+            rows += pieces[4 * p1++ + 3];
+        /* gather the chunk's rows (K-side and V-side latent + rope) */
+        double* gk = (double*)malloc((size_t)rows * ORC_D * sizeof(double));
+        double* gv = (double*)malloc((size_t)rows * ORC_L * sizeof(double));
+        int64_t at = 0;
+        for (int64_t p = p0; p < p1; ++p) {
+            const int b = (int)pieces[4 * p + 1];
+            const int32_t* bt = block_table + (int64_t)b * max_blocks;
+            for (int64_t j = 0; j < pieces[4 * p + 3]; ++j, ++at)
+                if (orc_fetch(&c, bt, pieces[4 * p + 2] + j, gk + at * ORC_D, gv + at * ORC_L) != 0) {
+                    bad = 1;
+                    for (int d = 0; d < ORC_D; ++d)
+                        gk[at * ORC_D + d] = 0.0;
+                    for (int d = 0; d < ORC_L; ++d)
+                        gv[at * ORC_L + d] = 0.0;
+                }
+        }
+        /* up-project every gathered row for every head */
+        double* kc = (double*)malloc((size_t)rows * H * KD * sizeof(double));
+        double* vc = (double*)malloc((size_t)rows * H * ORC_V * sizeof(double));
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t i = 0; i < rows * H; ++i) {
+            const int64_t j = i / H, h = i % H;
+            double* kk = kc + (h * rows + j) * KD;
+            orc_up_project(gk + j * ORC_D, gv + j * ORC_L, w_uk_t, w_uv, h, kk, vc + (h * rows + j) * ORC_V);
+            for (int e = 0; e < ORC_R; ++e)
+                kk[ORC_P + e] = gk[j * ORC_D + ORC_L + e];
+        }
+        /* every query of a request in this chunk attends to all of that request's rows here */
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t i = 0; i < total_q * H; ++i) {
+            const int64_t r = i / H, h = i % H;
+            const int b = req[r];
+            int64_t off = 0, n = 0;
+            for (int64_t p = p0; p < p1; ++p) {
+                if (pieces[4 * p + 1] == b) {
+                    n = pieces[4 * p + 3];
+                    break;
+                }
+                off += pieces[4 * p + 3];
+            }
+            if (n == 0)
+                continue; /* an empty partial carries no weight */
+            double qq[ORC_P + ORC_R], oc[ORC_V], lc;
+            for (int d = 0; d < KD; ++d)
+                qq[d] = oracle_bf16_value(q[(r * H + h) * KD + d]);
+            orc_mha_row(qq, kc + (h * rows + off) * KD, vc + (h * rows + off) * ORC_V, n, scale, oc, &lc);
+            orc_merge_pair(o + i * ORC_V, &lse[i], oc, lc, ORC_V);
+        }
+        free(gk);
+        free(gv);
+        free(kc);
+        free(vc);
+        p0 = p1;
+    }
+
+    /* ---- step 3: merge prefix and suffix ---- */
+    for (int64_t i = 0; i < total_q * H; ++i)
+        orc_merge_pair(o + i * ORC_V, &lse[i], o_suf + i * ORC_V, l_suf[i], ORC_V);
+    free(o_suf);
+    free(l_suf);
+    free(req);
+    free(pieces);
+    return bad ? -1 : 0;
+}
