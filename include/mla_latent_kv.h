@@ -235,6 +235,52 @@ mla_status mla_cache_write(const void* kv_c, int64_t kv_c_stride_t, const void* 
                            int64_t num_blocks, float kv_scale, int32_t* dev_status, mla_stream_t stream);
 
 /*
+ * Prefill, the compute-friendly route ([vLLM-MLA, Prefill section]; [vLLM-MLA, two-algorithms
+ * section]). A prefill request b has ctx_b tokens already in the paged cache (positions
+ * 0 .. ctx_b - 1) and q_b new tokens (positions ctx_b .. ctx_b + q_b - 1), packed request after
+ * request: request b owns rows [query_start_loc[b], query_start_loc[b + 1]) of q, kv_c and k_pe.
+ * Keys and values are up-projected per head, not absorbed:
+ *     k_j = [ c_j . W_UK_T[h]^T (128) || k_pe_j (64) ],   v_j = c_j . W_UV[h]  (128)
+ *     o[t, h, :] = sum_j softmax_j(scale * <q[t, h, :], k_j>) v_j,   lse[t, h] = ln sum_j exp(...)
+ * over the request's context and its new tokens 0 .. t (causal). Run as the page describes:
+ * the new tokens first (from kv_c / k_pe, not from the cache), then the context in chunks of at
+ * most chunk_rows gathered rows (each request's context cut at page boundaries; the plan of
+ * mla_prefill_chunk_plan), every chunk's partial result merged into the running one by LSE
+ * (merge_attn_states). FP8 rows are dequantised with k_scale on the key side (k_nope and k_pe)
+ * and v_scale on the value side.
+ *   q             bf16 [total_q, H, 192] contiguous: q_nope (128) || q_pe (64), RoPE applied
+ *   kv_c, k_pe    bf16 new-token rows, element (t, d) at kv_c[t * kv_c_stride_t + d] (d < 512),
+ *                 k_pe[t * k_pe_stride_t + r] (r < 64); strides multiples of 8
+ *   kv_cache      [num_blocks, 64, row] (bf16 or FP8 rows); only context rows are read
+ *   block_table   int32 [B, max_blocks], device; ctx_lens int32 [B] and query_start_loc int32
+ *                 [B + 1], device; ctx_lens_host / query_start_loc_host: the same values in host
+ *                 memory (they size the launches and the chunk plan; no device read-back)
+ *   W_UK_T        bf16 [H, 128, 512], W_UV bf16 [H, 512, 128] (the layouts of mla_absorb_q and
+ *                 mla_out_proj)
+ *   chunk_rows    context rows gathered and up-projected at a time, >= 64
+ *   workspace     >= mla_prefill_workspace_bytes(B, total_q, H, chunk_rows) bytes, 256-byte
+ *                 aligned, owned by the caller, contents undefined after the call
+ *   o             fp32 [total_q, H, 128]; lse fp32 [total_q, H] or NULL
+ * 1 <= H <= 128; 0 <= ctx_lens[b] <= max_blocks * 64. Bad block ids set MLA_DEV_BAD_BLOCK_ID,
+ * a device ctx_lens value outside that range MLA_DEV_SEQ_TOO_LONG. Pointers 16-byte aligned.
+ * Everything is enqueued on `stream`; nothing is allocated or synchronised.
+ */
+size_t mla_prefill_workspace_bytes(int B, int total_q, int H, int64_t chunk_rows);
+/* The context chunk plan: up to max_pieces rows of 4 int64 (chunk, request, first position,
+ * tokens), in order; returns the number of pieces (pieces may be NULL to count), or -1 for
+ * chunk_rows < 64. A request whose remaining context fits the open chunk goes in whole; else as
+ * many whole pages as fit; a chunk with no room for a page is closed. */
+int64_t mla_prefill_chunk_plan(const int32_t* ctx_lens_host, int B, int64_t chunk_rows, int64_t* pieces,
+                               int64_t max_pieces);
+mla_status mla_prefill(const void* q, const void* kv_c, int64_t kv_c_stride_t, const void* k_pe,
+                       int64_t k_pe_stride_t, const void* kv_cache, mla_kv_dtype kv_dtype, int64_t num_blocks,
+                       const int32_t* block_table, int max_blocks, const int32_t* ctx_lens,
+                       const int32_t* query_start_loc, const int32_t* ctx_lens_host,
+                       const int32_t* query_start_loc_host, int B, int H, const void* W_UK_T, const void* W_UV,
+                       float scale, int64_t chunk_rows, void* workspace, size_t workspace_bytes, float* o,
+                       float* lse, int32_t* dev_status, mla_stream_t stream);
+
+/*
  * mla_decode without a workspace argument, for callers that cannot allocate device memory when
  * they decode: serving loops that run under a fixed device-memory budget with every buffer made
  * at start-up, host runtimes that forbid device allocations after initialisation, and call paths

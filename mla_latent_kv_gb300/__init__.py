@@ -76,6 +76,12 @@ def lib() -> ctypes.CDLL:
         l.mla_cache_write.argtypes = [vp, i64, vp, i64, vp, i32, vp, i32, i64, f32, vp, vp]
         l.mla_out_proj.restype = i32
         l.mla_out_proj.argtypes = [vp, i32, vp, vp, i32, i32, i32, vp]
+        l.mla_prefill_workspace_bytes.restype = sz
+        l.mla_prefill_workspace_bytes.argtypes = [i32, i32, i32, i64]
+        l.mla_prefill_chunk_plan.restype = i64
+        l.mla_prefill_chunk_plan.argtypes = [vp, i32, i64, vp, i64]
+        l.mla_prefill.argtypes = [vp, vp, i64, vp, i64, vp, i32, i64, vp, i32, vp, vp, vp, vp, i32, i32, vp, vp,
+                                  f32, i64, vp, sz, vp, vp, vp, vp]
         _lib = l
         return l
 
@@ -247,3 +253,52 @@ def out_proj(o_latent, w_uv, out=None, out_dtype=DT_F32, stream=None):
                           device=o_latent.device)
     _check(lib().mla_out_proj(_p(o_latent), in_dtype, _p(w_uv), _p(out), out_dtype, T, H, _stream(stream)))
     return out
+
+
+def prefill_workspace_bytes(B: int, total_q: int, H: int, chunk_rows: int) -> int:
+    return int(lib().mla_prefill_workspace_bytes(B, total_q, H, int(chunk_rows)))
+
+
+def prefill_chunk_plan(ctx_lens, chunk_rows):
+    """The context chunk plan for host context lengths: a list of (chunk, request, first
+    position, tokens)."""
+    import numpy as np
+    cl = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    n = int(lib().mla_prefill_chunk_plan(cl.ctypes.data, cl.shape[0], int(chunk_rows), None, 0))
+    if n < 0:
+        raise MlaError(ERR_INVALID_ARG, "chunk_rows must hold at least one page")
+    out = np.zeros((max(n, 1), 4), np.int64)
+    lib().mla_prefill_chunk_plan(cl.ctypes.data, cl.shape[0], int(chunk_rows), out.ctypes.data, n)
+    return out[:n]
+
+
+def prefill(q, kv_c, k_pe, kv_cache, block_table, ctx_lens, query_start_loc, w_uk_t, w_uv, scale,
+            kv_dtype=KV_BF16, chunk_rows=8192, workspace=None, o=None, lse=None, dev_status=None, stream=None,
+            num_blocks=None):
+    """Prefill through the compute-friendly route. q [total_q, H, 192] bf16 (q_nope || q_pe),
+    kv_c [total_q, 512] / k_pe [total_q, 64] bf16 (the new tokens' rows, row-strided allowed),
+    ctx_lens [B] and query_start_loc [B + 1] int32 device tensors (read once on the host for the
+    launch plan) -> (o [total_q, H, 128] fp32, lse [total_q, H] fp32)."""
+    import torch
+    total_q, H = q.shape[0], q.shape[1]
+    B = int(query_start_loc.shape[0]) - 1
+    dev = q.device
+    ctx_host = ctx_lens.to("cpu", torch.int32).contiguous()
+    qsl_host = query_start_loc.to("cpu", torch.int32).contiguous()
+    if num_blocks is None:
+        num_blocks = kv_cache.numel() * kv_cache.element_size() // (PAGE * row_bytes(kv_dtype))
+    need = prefill_workspace_bytes(B, total_q, H, chunk_rows)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if o is None:
+        o = torch.empty((total_q, H, V), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((total_q, H), dtype=torch.float32, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().mla_prefill(_p(q), _p(kv_c), kv_c.stride(0) if total_q else L, _p(k_pe),
+                             k_pe.stride(0) if total_q else R, _p(kv_cache), kv_dtype, int(num_blocks),
+                             _p(block_table), block_table.shape[1], _p(ctx_lens), _p(query_start_loc),
+                             ctypes.c_void_p(ctx_host.data_ptr()), ctypes.c_void_p(qsl_host.data_ptr()), B, H,
+                             _p(w_uk_t), _p(w_uv), float(scale), int(chunk_rows), _p(workspace), ws_bytes, _p(o),
+                             _p(lse), _p(dev_status), _stream(stream)))
+    return o, lse

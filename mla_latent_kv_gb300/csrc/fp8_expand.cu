@@ -26,17 +26,6 @@ namespace {
 
 constexpr int kWarps = 8;
 
-// Two OCP E4M3 values (low byte first) -> two bf16 (low half first), exactly.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_bytes) {
-    uint32_t h2;
-    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h2) : "r"(two_bytes));
-    float lo, hi;
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(h2));
-    return ptx::pack_bf16x2(lo, hi);
-}
-
 __global__ void __launch_bounds__(kWarps * 32) fp8_expand_kernel(DecodeArgs p) {
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();  // it overwrites workspace the preceding kernel may still read
@@ -57,8 +46,8 @@ __global__ void __launch_bounds__(kWarps * 32) fp8_expand_kernel(DecodeArgs p) {
         // 72 eight-byte chunks of e4m3 (rows are 8-byte aligned: 584 = 73 * 8), then the scales
         for (int k = lane; k < 72; k += 32) {
             uint2 v = bad ? make_uint2(0, 0) : *reinterpret_cast<const uint2*>(src + 8 * k);
-            dst[k] = make_uint4(e4m3x2_to_bf16x2(v.x & 0xffffu), e4m3x2_to_bf16x2(v.x >> 16),
-                                e4m3x2_to_bf16x2(v.y & 0xffffu), e4m3x2_to_bf16x2(v.y >> 16));
+            dst[k] = make_uint4(ptx::e4m3x2_to_bf16x2(v.x & 0xffffu), ptx::e4m3x2_to_bf16x2(v.x >> 16),
+                                ptx::e4m3x2_to_bf16x2(v.y & 0xffffu), ptx::e4m3x2_to_bf16x2(v.y >> 16));
         }
         if (lane == 0) {
             float2 sc = make_float2(0.f, 0.f);

@@ -7,6 +7,9 @@
 //              [TRT-TP, absorption section]: fused_q = [q_nope W_kb^T || q_pe])
 //   out_proj: o[t, h, :]        = o_latent[t, h, :] . W_UV[h]       (K = 512, M = 128)
 //             ([vLLM-MLA, two-algorithms section]: the V up-projection after the latent kernel)
+//   up_proj:  k_nope[j, h, :]   = c[j, :] . W_UK_T[h]^T, v[j, h, :] = c[j, :] . W_UV[h]
+//             (K = 512, M = 128; [vLLM-MLA, Prefill section]: kv_b_proj of the gathered latent
+//              rows; the activation row is shared by all heads, and W_UK_T[h] is read K-major)
 //
 // Both are D[t, h, m] = sum_k W[h][k][m] * X[t, h, k] with the weights stored [H][K][M] (m
 // fastest) and few tokens T (decode batches). The kernel runs them "swap-AB": the MMA's M side is
@@ -66,6 +69,8 @@ struct HeadGemmArgs {
     int64_t out_st, out_sh;
     const uint16_t* q_pe;    // absorb only (may be null): copied to out[t, h, 512:576] by m tile 0
     int64_t pe_st, pe_sh;
+    int x_shared;            // one activation row per token, used by every head (up_proj)
+    int w_kmajor;            // weights stored [H][M][K] (k fastest) instead of [H][K][M]
 };
 
 struct Unit {
@@ -141,6 +146,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
             tma_prefetch_desc(&w_map);
             tma_prefetch_desc(&x_map);
+            // one 128 (m) x 64 (k) weight tile as two 64-row boxes: [K][M] layout boxes are
+            // 64 m wide at k rows c*64.., [M][K] layout boxes are 64 k wide at m rows mt*128..
+            auto load_w = [&](uint32_t dst, uint32_t bar, const Unit& u, int c) {
+                if (p.w_kmajor) {
+                    const int wy = u.h * p.M_total + u.mt * 128;
+                    tma_load_2d(dst, &w_map, bar, c * kKChunk, wy);
+                    tma_load_2d(dst + kWBox, &w_map, bar, c * kKChunk, wy + 64);
+                } else {
+                    const int wy = u.h * p.K + c * kKChunk;
+                    tma_load_2d(dst, &w_map, bar, u.mt * 128, wy);
+                    tma_load_2d(dst + kWBox, &w_map, bar, u.mt * 128 + 64, wy);
+                }
+            };
             // The weights of the first unit's first stages go out before the preceding kernel
             // (which may be writing the activations, or still reading this kernel's output)
             // has finished; everything else waits for it.
@@ -151,9 +169,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int c = 0; c < pre; ++c) {
                     const uint32_t dst = sbase + c * stage_bytes;
                     bar_arrive_expect_tx(FULL(c), stage_bytes);
-                    const int wy = w0.h * p.K + c * kKChunk;
-                    tma_load_2d(dst, &w_map, FULL(c), w0.mt * 128, wy);
-                    tma_load_2d(dst + kWBox, &w_map, FULL(c), w0.mt * 128 + 64, wy);
+                    load_w(dst, FULL(c), w0, c);
                     last[c] = c;
                 }
             }
@@ -171,15 +187,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const uint32_t dst = sbase + s * stage_bytes;
                     if (g >= pre) {  // the first `pre` stages' weights are already on their way
                         bar_arrive_expect_tx(FULL(s), stage_bytes);
-                        const int wy = w.h * p.K + c * kKChunk;
-                        tma_load_2d(dst, &w_map, FULL(s), w.mt * 128, wy);
-                        tma_load_2d(dst + kWBox, &w_map, FULL(s), w.mt * 128 + 64, wy);
+                        load_w(dst, FULL(s), w, c);
                     }
+                    const int xh = p.x_shared ? 0 : w.h;
                     if (p.x_f32) {
-                        tma_load_3d(dst + kWStage, &x_map, FULL(s), c * kKChunk, w.h, w.nt * NT);
-                        tma_load_3d(dst + kWStage + x_panel, &x_map, FULL(s), c * kKChunk + 32, w.h, w.nt * NT);
+                        tma_load_3d(dst + kWStage, &x_map, FULL(s), c * kKChunk, xh, w.nt * NT);
+                        tma_load_3d(dst + kWStage + x_panel, &x_map, FULL(s), c * kKChunk + 32, xh, w.nt * NT);
                     } else {
-                        tma_load_3d(dst + kWStage, &x_map, FULL(s), c * kKChunk, w.h, w.nt * NT);
+                        tma_load_3d(dst + kWStage, &x_map, FULL(s), c * kKChunk, xh, w.nt * NT);
                     }
                     last[s] = g;
                 }
@@ -193,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     } else if (warp == 5) {
         // ---- MMA issuer -----------------------------------------------------------------
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(128, NT, true, false);
+            const uint32_t idesc = idesc_bf16_f32(128, NT, !p.w_kmajor, false);
             int g = 0, i = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
@@ -216,7 +231,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const uint32_t xb = wb + kWStage;
 #pragma unroll
                     for (int kk = 0; kk < kKChunk / 16; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(wb + kk * 2048, kWBox, 1024);
+                        // A = W^T: MN-major (two 64-m boxes, 16 k rows per step) or K-major
+                        // (128 m rows of 128 bytes, 32 bytes per step)
+                        const uint64_t ad = p.w_kmajor ? smem_desc_sw128(wb + kk * 32, 16, 1024)
+                                                       : smem_desc_sw128(wb + kk * 2048, kWBox, 1024);
                         mma_ss(d, ad, smem_desc_sw128(xb + kk * 32, 16, 1024), idesc, (c | kk) != 0);
                         if (p.x_f32) mma_ss(d, ad, smem_desc_sw128(xb + x_panel + kk * 32, 16, 1024), idesc, 1u);
                     }
@@ -368,18 +386,20 @@ cudaError_t launch_head_gemm(HeadGemmArgs a, const uint16_t* w, const void* x, i
                              cudaStream_t s) {
     CUtensorMap wmap, xmap;
     {
-        const uint64_t dims[2] = {(uint64_t)a.M_total, (uint64_t)a.H * a.K};
-        const uint64_t strides[1] = {(uint64_t)a.M_total * 2};
+        const uint64_t dims[2] = {a.w_kmajor ? (uint64_t)a.K : (uint64_t)a.M_total,
+                                  a.w_kmajor ? (uint64_t)a.H * a.M_total : (uint64_t)a.H * a.K};
+        const uint64_t strides[1] = {dims[0] * 2};
         const uint32_t box[2] = {64, 64};
         cudaError_t e = encode_tmap(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, dims, strides, box, true);
         if (e != cudaSuccess) return e;
     }
     {
         const uint64_t es = a.x_f32 ? 4 : 2;
+        const int xh = a.x_shared ? 1 : a.H;
         // A stride of a dimension of extent 1 is never used; give it a harmless legal value.
-        if (a.H == 1) x_sh = a.K;
-        if (a.T == 1) x_st = x_sh * a.H;
-        const uint64_t dims[3] = {(uint64_t)a.K, (uint64_t)a.H, (uint64_t)a.T};
+        if (xh == 1) x_sh = a.K;
+        if (a.T == 1) x_st = x_sh * xh;
+        const uint64_t dims[3] = {(uint64_t)a.K, (uint64_t)xh, (uint64_t)a.T};
         const uint64_t strides[2] = {(uint64_t)x_sh * es, (uint64_t)x_st * es};
         const uint32_t box[3] = {a.x_f32 ? 32u : 64u, 1u, (uint32_t)a.n_tile};
         cudaError_t e = encode_tmap(&xmap, a.x_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -456,6 +476,29 @@ cudaError_t launch_out_proj_sm103(const void* o_latent, int in_dtype, const uint
     a.out_sh = kV;
     a.q_pe = nullptr;
     return launch_head_gemm(a, w_uv, o_latent, (int64_t)H * kL, kL, s);
+}
+
+// Up-projection of gathered latent rows: out[j, h, m] = sum_l x[j, l] * W[h] with W_UK_T[h]
+// ([H][128][512], K-major) for k_nope or W_UV[h] ([H][512][128]) for v; x [rows, 512] bf16
+// with row stride x_st; out [rows, H, 128] bf16.
+cudaError_t launch_up_proj_sm103(const uint16_t* x, int64_t x_st, int rows, const uint16_t* w, bool w_is_uk,
+                                 uint16_t* out, int H, cudaStream_t s) {
+    HeadGemmArgs a{};
+    a.T = rows;
+    a.H = H;
+    a.K = kL;
+    a.M_total = 128;
+    a.n_tile = pick_n_tile(rows);
+    a.stages = kStages;
+    a.x_f32 = 0;
+    a.out = out;
+    a.out_f32 = 0;
+    a.out_st = (int64_t)H * 128;
+    a.out_sh = 128;
+    a.q_pe = nullptr;
+    a.x_shared = 1;
+    a.w_kmajor = w_is_uk ? 1 : 0;
+    return launch_head_gemm(a, w, x, x_st, kL, s);
 }
 
 }  // namespace mla

@@ -147,5 +147,59 @@ cudaError_t launch_absorb_sm103(const uint16_t* q_nope, int64_t snt, int64_t snh
                                 cudaStream_t s);
 cudaError_t launch_out_proj_sm103(const void* o_latent, int in_dtype, const uint16_t* w_uv, void* o,
                                   int out_dtype, int T, int H, cudaStream_t s);
+cudaError_t launch_up_proj_sm103(const uint16_t* x, int64_t x_st, int rows, const uint16_t* w, bool w_is_uk,
+                                 uint16_t* out, int H, cudaStream_t s);
+
+// ---- prefill, the compute-friendly route ---------------------------------------------------
+// Rows of one segment (the new tokens, or one context chunk) gathered into a contiguous
+// workspace: the latent part x [rows, 512] and the rope part kpe [rows, 64], both bf16 holding
+// the stored values exactly (FP8 codes are not scaled here), plus per-row (k_scale, v_scale)
+// for an FP8 cache.
+struct PrefillGather {
+    const uint16_t* kv_c;       // new tokens: rows come from kv_c / k_pe (row strides st_c, st_pe)
+    int64_t st_c;
+    const uint16_t* k_pe;
+    int64_t st_pe;
+    const uint8_t* cache;       // context chunk: packed context rows [c0, c0 + rows)
+    int kv_dtype;
+    int64_t num_blocks;
+    const int32_t* block_table;
+    int max_blocks;
+    const int32_t* cu_ctx;      // [B + 1] prefix sums of the context lengths
+    int B;
+    int64_t c0;
+    int rows;
+    uint16_t* x;
+    uint16_t* kpe;
+    float2* scales;             // FP8 only
+    int32_t* dev_status;
+};
+
+// One attention segment: every query row of the requests attends to its keys in the segment.
+// causal: the keys are the request's own new tokens (key i visible to query row t iff i <= t);
+// otherwise the keys are the request's rows of the context chunk [c0, c1) (all visible). The
+// result is written (merge = 0) or merged by LSE into o / lse (merge = 1).
+struct PrefillAttn {
+    const uint16_t* q;          // [T, H, 192]
+    const uint16_t* kn;         // [key_rows, H, 128] up-projected k_nope
+    const uint16_t* v;          // [key_rows, H, 128] up-projected v
+    const uint16_t* kpe;        // [key_rows, 64]
+    const float2* scales;       // FP8 only: per key row (k_scale, v_scale)
+    int key_rows;
+    const int32_t* qsl;         // [B + 1]
+    const int32_t* cu_ctx;      // [B + 1]
+    int B, H, T, max_q_len;
+    int causal;
+    int64_t c0, c1;
+    float scale;
+    int merge;
+    float* o;                   // [T, H, 128]
+    float* lse;                 // [T, H]
+    int32_t* dev_status;
+};
+cudaError_t launch_prefill_cu_ctx(const int32_t* ctx_lens, int B, int32_t* cu_ctx, int32_t* dev_status,
+                                  cudaStream_t s);
+cudaError_t launch_prefill_gather(const PrefillGather& g, cudaStream_t s);
+cudaError_t launch_prefill_attn(const PrefillAttn& a, cudaStream_t s);
 
 }  // namespace mla

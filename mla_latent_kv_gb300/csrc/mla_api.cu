@@ -11,6 +11,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <vector>
 
 #include "internal.h"
 
@@ -366,6 +367,238 @@ mla_status mla_out_proj(const void* o_latent, mla_dtype in_dtype, const void* W_
     cudaError_t e = mla::launch_out_proj_sm103(o_latent, in_dtype, (const uint16_t*)W_UV, o, out_dtype, T, H,
                                               (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "mla_out_proj launch");
+    return ok();
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// Prefill (compute-friendly route)
+// ---------------------------------------------------------------------------------------------
+namespace {
+
+struct PrefillLayout {
+    size_t cu_ctx, x, kpe, scales, kn, v, lse, total;
+    int64_t rows;  // rows of one segment's workspace
+};
+
+PrefillLayout prefill_layout(int B, int total_q, int H, int64_t chunk_rows) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    PrefillLayout w{};
+    w.rows = std::max<int64_t>(total_q, chunk_rows);
+    size_t off = 0;
+    w.cu_ctx = off;
+    off += up((size_t)(B + 1) * sizeof(int32_t));
+    w.x = off;
+    off += up((size_t)w.rows * mla::kL * 2);
+    w.kpe = off;
+    off += up((size_t)w.rows * mla::kR * 2);
+    w.scales = off;
+    off += up((size_t)w.rows * 2 * sizeof(float));
+    w.kn = off;
+    off += up((size_t)w.rows * H * 128 * 2);
+    w.v = off;
+    off += up((size_t)w.rows * H * 128 * 2);
+    w.lse = off;
+    off += up((size_t)total_q * H * sizeof(float));
+    w.total = off;
+    return w;
+}
+
+// The chunk rule, walked over the host copy of the context lengths; calls emit(chunk, b, pos, n).
+template <class F>
+void plan_chunks(const int32_t* ctx, int B, int64_t budget, F&& emit) {
+    int64_t chunk = 0, used = 0;
+    for (int b = 0; b < B; ++b) {
+        const int64_t len = ctx[b] > 0 ? ctx[b] : 0;
+        int64_t pos = 0;
+        while (pos < len) {
+            int64_t n = len - pos;
+            const int64_t room = budget - used;
+            if (n > room) {
+                n = room / mla::kPage * mla::kPage;  // whole pages only, so the next piece starts on one
+                if (n == 0) {
+                    ++chunk;
+                    used = 0;
+                    continue;
+                }
+            }
+            emit(chunk, b, pos, n);
+            used += n;
+            pos += n;
+        }
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mla_prefill_workspace_bytes(int B, int total_q, int H, int64_t chunk_rows) {
+    if (B < 1 || total_q < 0 || H < 1 || H > MLA_MAX_HEADS || chunk_rows < mla::kPage) return 0;
+    return prefill_layout(B, total_q, H, chunk_rows).total;
+}
+
+int64_t mla_prefill_chunk_plan(const int32_t* ctx_lens_host, int B, int64_t chunk_rows, int64_t* pieces,
+                               int64_t max_pieces) {
+    if (chunk_rows < mla::kPage || B < 0 || (B > 0 && !ctx_lens_host)) return -1;
+    int64_t n = 0;
+    plan_chunks(ctx_lens_host, B, chunk_rows, [&](int64_t c, int b, int64_t pos, int64_t len) {
+        if (pieces && n < max_pieces) {
+            pieces[4 * n] = c;
+            pieces[4 * n + 1] = b;
+            pieces[4 * n + 2] = pos;
+            pieces[4 * n + 3] = len;
+        }
+        ++n;
+    });
+    return n;
+}
+
+mla_status mla_prefill(const void* q, const void* kv_c, int64_t kv_c_stride_t, const void* k_pe,
+                       int64_t k_pe_stride_t, const void* kv_cache, mla_kv_dtype kv_dtype, int64_t num_blocks,
+                       const int32_t* block_table, int max_blocks, const int32_t* ctx_lens,
+                       const int32_t* query_start_loc, const int32_t* ctx_lens_host,
+                       const int32_t* query_start_loc_host, int B, int H, const void* W_UK_T, const void* W_UV,
+                       float scale, int64_t chunk_rows, void* workspace, size_t workspace_bytes, float* o,
+                       float* lse, int32_t* dev_status, mla_stream_t stream) {
+    if (B < 1) return fail(MLA_ERR_INVALID_ARG, "mla_prefill: B=%d < 1", B);
+    if (H < 1 || H > MLA_MAX_HEADS)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_prefill: H=%d outside [1, %d]", H, MLA_MAX_HEADS);
+    if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3_SCALED)
+        return fail(MLA_ERR_INVALID_ARG, "mla_prefill: unknown kv_dtype %d", (int)kv_dtype);
+    if (chunk_rows < mla::kPage)
+        return fail(MLA_ERR_INVALID_ARG, "mla_prefill: chunk_rows=%lld < 64", (long long)chunk_rows);
+    if (chunk_rows > ((int64_t)1 << 24))
+        return fail(MLA_ERR_UNSUPPORTED, "mla_prefill: chunk_rows=%lld above 2^24", (long long)chunk_rows);
+    if (!(scale > 0.f) || std::isinf(scale))
+        return fail(MLA_ERR_INVALID_ARG, "mla_prefill: scale must be finite and > 0");
+    if (!ctx_lens_host || !query_start_loc_host) return fail(MLA_ERR_INVALID_ARG, "mla_prefill: null host metadata");
+    if (query_start_loc_host[0] != 0) return fail(MLA_ERR_INVALID_ARG, "mla_prefill: query_start_loc[0] != 0");
+    if (num_blocks < 0 || max_blocks < 0)
+        return fail(MLA_ERR_INVALID_ARG, "mla_prefill: negative num_blocks/max_blocks");
+    int max_q = 0;
+    int64_t total_ctx = 0;
+    for (int b = 0; b < B; ++b) {
+        const int ql = query_start_loc_host[b + 1] - query_start_loc_host[b];
+        if (ql < 0) return fail(MLA_ERR_INVALID_ARG, "mla_prefill: query_start_loc decreases at %d", b);
+        max_q = std::max(max_q, ql);
+        if (ctx_lens_host[b] < 0 || (int64_t)ctx_lens_host[b] > (int64_t)max_blocks * mla::kPage)
+            return fail(MLA_ERR_INVALID_ARG, "mla_prefill: ctx_lens[%d]=%d outside [0, max_blocks*64]", b,
+                        ctx_lens_host[b]);
+        total_ctx += ctx_lens_host[b];
+    }
+    const int total_q = query_start_loc_host[B];
+    if (total_ctx > INT32_MAX)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_prefill: %lld context rows too many", (long long)total_ctx);
+    if (total_q == 0) return ok();
+    if (!q || !kv_c || !k_pe || !ctx_lens || !query_start_loc || !W_UK_T || !W_UV || !o || !workspace ||
+        (total_ctx > 0 && (!kv_cache || !block_table)))
+        return fail(MLA_ERR_INVALID_ARG, "mla_prefill: null pointer");
+    if (!aligned16(q) || !aligned16(kv_c) || !aligned16(k_pe) || !aligned16(W_UK_T) || !aligned16(W_UV) ||
+        !aligned16(o) || (kv_cache && !aligned16(kv_cache)))
+        return fail(MLA_ERR_UNSUPPORTED, "mla_prefill: pointers must be 16-byte aligned");
+    if (kv_c_stride_t < mla::kL || k_pe_stride_t < mla::kR || kv_c_stride_t % 8 || k_pe_stride_t % 8)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_prefill: row strides must be multiples of 8 covering the row");
+    const PrefillLayout L = prefill_layout(B, total_q, H, chunk_rows);
+    if (workspace_bytes < L.total)
+        return fail(MLA_ERR_WORKSPACE_TOO_SMALL, "mla_prefill: workspace %zu < %zu bytes", workspace_bytes, L.total);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(MLA_ERR_UNSUPPORTED, "mla_prefill: workspace must be 256-byte aligned");
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int32_t* cu_ctx = reinterpret_cast<int32_t*>(ws + L.cu_ctx);
+    uint16_t* x = reinterpret_cast<uint16_t*>(ws + L.x);
+    uint16_t* kpe = reinterpret_cast<uint16_t*>(ws + L.kpe);
+    float2* scales = reinterpret_cast<float2*>(ws + L.scales);
+    uint16_t* kn = reinterpret_cast<uint16_t*>(ws + L.kn);
+    uint16_t* vv = reinterpret_cast<uint16_t*>(ws + L.v);
+    float* lse_out = lse ? lse : reinterpret_cast<float*>(ws + L.lse);
+    const cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = mla::launch_prefill_cu_ctx(ctx_lens, B, cu_ctx, dev_status, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mla_prefill prefix-sum launch");
+
+    mla::PrefillAttn a{};
+    a.q = static_cast<const uint16_t*>(q);
+    a.kn = kn;
+    a.v = vv;
+    a.kpe = kpe;
+    a.qsl = query_start_loc;
+    a.cu_ctx = cu_ctx;
+    a.B = B;
+    a.H = H;
+    a.T = total_q;
+    a.max_q_len = max_q;
+    a.scale = scale;
+    a.o = o;
+    a.lse = lse_out;
+    a.dev_status = dev_status;
+    // one segment: gather, the two up-projections, attention
+    auto segment = [&](const mla::PrefillGather& g, bool fp8) -> mla_status {
+        cudaError_t err = mla::launch_prefill_gather(g, s);
+        if (err != cudaSuccess) return cuda_fail(err, "mla_prefill gather launch");
+        err = mla::launch_up_proj_sm103(x, mla::kL, g.rows, static_cast<const uint16_t*>(W_UK_T), true, kn, H, s);
+        if (err != cudaSuccess) return cuda_fail(err, "mla_prefill k up-projection launch");
+        err = mla::launch_up_proj_sm103(x, mla::kL, g.rows, static_cast<const uint16_t*>(W_UV), false, vv, H, s);
+        if (err != cudaSuccess) return cuda_fail(err, "mla_prefill v up-projection launch");
+        a.key_rows = g.rows;
+        a.scales = fp8 ? scales : nullptr;
+        err = mla::launch_prefill_attn(a, s);
+        if (err != cudaSuccess) return cuda_fail(err, "mla_prefill attention launch");
+        return MLA_OK;
+    };
+    // 1. the new tokens, causal among themselves
+    {
+        mla::PrefillGather g{};
+        g.kv_c = static_cast<const uint16_t*>(kv_c);
+        g.st_c = kv_c_stride_t;
+        g.k_pe = static_cast<const uint16_t*>(k_pe);
+        g.st_pe = k_pe_stride_t;
+        g.rows = total_q;
+        g.x = x;
+        g.kpe = kpe;
+        a.causal = 1;
+        a.merge = 0;
+        const mla_status st = segment(g, false);
+        if (st != MLA_OK) return st;
+    }
+    // 2. the context, chunk by chunk, merged into the running result
+    std::vector<int64_t> cu_host((size_t)B + 1, 0);
+    for (int b = 0; b < B; ++b) cu_host[b + 1] = cu_host[b] + ctx_lens_host[b];
+    int64_t cur = -1, c0 = 0, c1 = 0;
+    mla_status st = MLA_OK;
+    auto flush = [&]() {
+        if (cur < 0 || st != MLA_OK) return;
+        mla::PrefillGather g{};
+        g.cache = static_cast<const uint8_t*>(kv_cache);
+        g.kv_dtype = kv_dtype;
+        g.num_blocks = num_blocks;
+        g.block_table = block_table;
+        g.max_blocks = max_blocks;
+        g.cu_ctx = cu_ctx;
+        g.B = B;
+        g.c0 = c0;
+        g.rows = (int)(c1 - c0);
+        g.x = x;
+        g.kpe = kpe;
+        g.scales = scales;
+        g.dev_status = dev_status;
+        a.causal = 0;
+        a.merge = 1;
+        a.c0 = c0;
+        a.c1 = c1;
+        st = segment(g, kv_dtype == MLA_KV_FP8_E4M3_SCALED);
+    };
+    plan_chunks(ctx_lens_host, B, chunk_rows, [&](int64_t c, int b, int64_t pos, int64_t n) {
+        if (c != cur) {
+            flush();
+            cur = c;
+            c0 = cu_host[b] + pos;
+        }
+        c1 = cu_host[b] + pos + n;
+    });
+    flush();
+    if (st != MLA_OK) return st;
     return ok();
 }
 

@@ -1,0 +1,533 @@
+// prefill_sm103.cu -- the prefill ("compute-friendly") route of MLA on the 5th-generation tensor
+// cores ([vLLM-MLA, Prefill section]).
+//
+// A prefill request b has ctx_b tokens in the paged cache and q_b new tokens. Keys and values are
+// not absorbed: every latent row c_j is up-projected per head, k_j = [c_j W_UK (128) || k_pe_j
+// (64)], v_j = c_j W_UV (128), and attention is standard MHA with a 192-dim q.k and a 128-dim
+// output. The route runs as segments, each one gather -> two up-projection GEMMs (gemm_sm103.cu)
+// -> attention (this file):
+//   1. the new tokens, attending causally among themselves; the result is written;
+//   2. the context, in chunks of at most chunk_rows gathered rows; each chunk's result is merged
+//      into the running one by LSE in the attention kernel's epilogue (merge_attn_states).
+//
+// Attention kernel: one CTA per (128-query tile, request, head), 192 threads, 1 CTA per SM.
+//   warp 4 lane 0   TMA: the q tile (three 64-dim panels); per 128-key tile the K panels
+//                   (k_nope dims 0-63 and 64-127 of this head, k_pe shared by all heads) into a
+//                   2-stage ring and, one tile behind, the two V panels into another 2-stage ring
+//   warp 5 lane 0   tcgen05.mma: S_j = Q K_j^T (M = 128 queries, N = 128 keys, K = 192) into one
+//                   of three 128-column TMEM buffers, then O += P_{j-1} V_{j-1} with P read from
+//                   TMEM (M = 128, N = 128 dims, K = 128 keys; V is an MN-major operand)
+//   warps 0-3       softmax, one query row per thread (its TMEM lane): fp32 online softmax in the
+//                   exp2 domain with a lazily moved running max (O and l are rescaled only when a
+//                   row's max grows by more than 2^8); P goes back over S as bf16; at the end
+//                   O / l and the LSE, merged with the result of the earlier segments
+// FP8 cache: the gathered rows hold the e4m3 values unscaled; k_scale multiplies the key's logit
+// column and v_scale its P column, which is exact because the up-projection is linear.
+// TMEM: S buffers at columns 0, 128, 256; O at 384..511. Every wait is bounded.
+#include <cuda.h>
+#include <math_constants.h>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+
+namespace mla {
+
+cudaError_t encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                        const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                        bool swizzle128);
+
+namespace {
+
+using namespace ptx;
+
+// ---------------------------------------------------------------- context prefix sums
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads)
+    cu_ctx_kernel(const int32_t* __restrict__ ctx_lens, int B, int32_t cap, int32_t* __restrict__ cu,
+                  int32_t* dev_status) {
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    griddep_wait();
+    __shared__ int32_t part[kScanThreads];
+    const int per = (B + kScanThreads - 1) / kScanThreads;
+    const int b0 = threadIdx.x * per;
+    auto len = [&](int b) {
+        int32_t n = ctx_lens[b];
+        if (n < 0 || n > cap) {
+            if (dev_status) atomicOr(dev_status, MLA_DEV_SEQ_TOO_LONG);
+            n = n < 0 ? 0 : cap;
+        }
+        return n;
+    };
+    int32_t sum = 0;
+    for (int b = b0; b < b0 + per && b < B; ++b) sum += len(b);
+    part[threadIdx.x] = sum;
+    __syncthreads();
+    for (int off = 1; off < kScanThreads; off <<= 1) {  // inclusive scan
+        const int32_t v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int32_t run = threadIdx.x > 0 ? part[threadIdx.x - 1] : 0;
+    for (int b = b0; b < b0 + per && b < B; ++b) {
+        cu[b] = run;
+        run += len(b);
+    }
+    if (threadIdx.x == kScanThreads - 1) cu[B] = part[kScanThreads - 1];
+}
+
+// ---------------------------------------------------------------- gather
+// One warp per row: 64 16-byte chunks of latent and 8 of rope (bf16), or 72 8-byte chunks of e4m3
+// widened to bf16 plus the row's two scales.
+constexpr int kGatherWarps = 8;
+
+__global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(PrefillGather g) {
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    griddep_wait();  // the workspace may still be read by the previous segment's kernels
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i = blockIdx.x * kGatherWarps + warp;
+    if (i >= g.rows) return;
+    uint4* const xd = reinterpret_cast<uint4*>(g.x + (int64_t)i * kL);
+    uint4* const pd = reinterpret_cast<uint4*>(g.kpe + (int64_t)i * kR);
+    if (g.kv_c != nullptr) {  // the new tokens' own rows
+        const uint4* xs = reinterpret_cast<const uint4*>(g.kv_c + (int64_t)i * g.st_c);
+        const uint4* ps = reinterpret_cast<const uint4*>(g.k_pe + (int64_t)i * g.st_pe);
+        const uint4 a = xs[lane], b = xs[lane + 32];
+        xd[lane] = a;
+        xd[lane + 32] = b;
+        if (lane < 8) pd[lane] = ps[lane];
+        return;
+    }
+    // packed context row -> (request, position): the last request whose first row is <= it
+    const int64_t gr = g.c0 + i;
+    int lo = 0, hi = g.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (g.cu_ctx[mid] <= gr)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int64_t pos = gr - g.cu_ctx[lo];
+    const int64_t blk = g.block_table[(int64_t)lo * g.max_blocks + pos / kPage];
+    if (blk < 0 || blk >= g.num_blocks) {
+        if (lane == 0 && g.dev_status) atomicOr(g.dev_status, MLA_DEV_BAD_BLOCK_ID);
+        xd[lane] = make_uint4(0, 0, 0, 0);
+        xd[lane + 32] = make_uint4(0, 0, 0, 0);
+        if (lane < 8) pd[lane] = make_uint4(0, 0, 0, 0);
+        if (lane == 0 && g.scales) g.scales[i] = make_float2(0.f, 0.f);
+        return;
+    }
+    const int64_t slot = blk * kPage + pos % kPage;
+    if (g.kv_dtype == MLA_KV_BF16) {
+        const uint4* src = reinterpret_cast<const uint4*>(g.cache + slot * kBf16RowBytes);
+        const uint4 a = src[lane], b = src[lane + 32];
+        uint4 c = make_uint4(0, 0, 0, 0);
+        if (lane < 8) c = src[64 + lane];
+        xd[lane] = a;
+        xd[lane + 32] = b;
+        if (lane < 8) pd[lane] = c;
+    } else {
+        const uint8_t* row = g.cache + slot * kFp8RowBytes;  // 584-byte rows are 8-byte aligned
+        uint2 v[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+            if (lane + 32 * k < 72) v[k] = *reinterpret_cast<const uint2*>(row + 8 * (lane + 32 * k));
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const int c = lane + 32 * k;
+            if (c >= 72) continue;
+            const uint4 o = make_uint4(e4m3x2_to_bf16x2(v[k].x & 0xffffu), e4m3x2_to_bf16x2(v[k].x >> 16),
+                                       e4m3x2_to_bf16x2(v[k].y & 0xffffu), e4m3x2_to_bf16x2(v[k].y >> 16));
+            if (c < 64)
+                xd[c] = o;
+            else
+                pd[c - 64] = o;
+        }
+        if (lane == 0) g.scales[i] = *reinterpret_cast<const float2*>(row + kD);
+    }
+}
+
+// ---------------------------------------------------------------- attention
+constexpr int kAttnThreads = 192;        // warps 0-3 softmax, 4 TMA + TMEM, 5 MMA
+constexpr int kPanel = 128 * 128;        // 128 rows x 64 bf16 with the 128-byte swizzle: 16 KB
+constexpr int OFF_Q = 0;                 // 3 panels
+constexpr int OFF_K = 3 * kPanel;        // 2 stages x 3 panels
+constexpr int OFF_V = 9 * kPanel;        // 2 stages x 2 panels
+constexpr int OFF_SC = 13 * kPanel;      // FP8: 2 x 128 (k_scale, v_scale)
+constexpr int kAttnSmem = OFF_SC + 2 * 128 * 8 + 1024;  // + 1024-byte alignment slack
+constexpr uint32_t kOCol = 384;
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
+constexpr uint32_t kBarScales = 1;       // named barrier of the softmax warps
+enum {
+    B_Q = 0,
+    B_KFULL = 1,    // 2
+    B_KEMPTY = 3,   // 2
+    B_VFULL = 5,    // 2
+    B_VEMPTY = 7,   // 2
+    B_SFULL = 9,    // 3
+    B_PREADY = 12,  // 3
+    B_PVDONE = 15,  // 3
+    B_FINAL = 18,
+    kNumBars = 19
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* ds) {
+    const bool ok = wait_bar(bar, parity, abort, ds);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kn_map,
+                const __grid_constant__ CUtensorMap kpe_map, const __grid_constant__ CUtensorMap v_map,
+                const PrefillAttn p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[kNumBars];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    griddep_wait();  // q, the up-projected keys and the running o / lse come from earlier kernels
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.y, h = blockIdx.z;
+    const int q_begin = p.qsl[b];
+    const int q_len = p.qsl[b + 1] - q_begin;
+    const int r0 = blockIdx.x * 128;  // first query row of the tile, within the request
+    if (r0 >= q_len) return;
+    int64_t key0;  // first key row in the segment's workspace
+    int n_keys;
+    if (p.causal) {
+        key0 = q_begin;
+        n_keys = min(q_len, r0 + 128);  // the tile's last row sees new tokens 0 .. r0 + 127
+    } else {
+        const int64_t g0 = max(p.c0, (int64_t)p.cu_ctx[b]);
+        const int64_t g1 = min(p.c1, (int64_t)p.cu_ctx[b + 1]);
+        if (g1 <= g0) return;  // no context of this request in the chunk: nothing to merge
+        key0 = g0 - p.c0;
+        n_keys = (int)(g1 - g0);
+    }
+    const int n_tiles = (n_keys + 127) / 128;
+
+    const uint32_t sbase = (smem_addr(smem_raw) + 1023u) & ~1023u;
+    uint8_t* const sgen = smem_raw + (sbase - smem_addr(smem_raw));
+    const uint32_t bar0 = smem_addr(&bars[0]);
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    int32_t* const ds = p.dev_status;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        bar_init(bar(B_Q), 1);
+        for (int i = 0; i < 2; ++i) {
+            bar_init(bar(B_KFULL + i), 1);
+            bar_init(bar(B_KEMPTY + i), 1);
+            bar_init(bar(B_VFULL + i), 1);
+            bar_init(bar(B_VEMPTY + i), 1);
+        }
+        for (int i = 0; i < 3; ++i) {
+            bar_init(bar(B_SFULL + i), 1);
+            bar_init(bar(B_PREADY + i), 128);
+            bar_init(bar(B_PVDONE + i), 1);
+        }
+        bar_init(bar(B_FINAL), 1);
+        fence_barrier_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(smem_addr(&tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    volatile int* abort = &abort_flag;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&q_map);
+            tma_prefetch_desc(&kn_map);
+            tma_prefetch_desc(&kpe_map);
+            tma_prefetch_desc(&v_map);
+            bar_arrive_expect_tx(bar(B_Q), 3 * kPanel);
+            for (int pn = 0; pn < 3; ++pn)
+                tma_load_3d(sbase + OFF_Q + pn * kPanel, &q_map, bar(B_Q), 64 * pn, h, q_begin + r0);
+            int klast[2] = {-1, -1}, vlast[2] = {-1, -1};
+            auto load_v = [&](int j) -> bool {
+                const int s = j & 1;
+                if (j >= 2 && !wait_bar(bar(B_VEMPTY + s), ((j >> 1) - 1) & 1, abort, ds)) return false;
+                const uint32_t dst = sbase + OFF_V + s * 2 * kPanel;
+                const int z = (int)(key0 + 128 * j);
+                bar_arrive_expect_tx(bar(B_VFULL + s), 2 * kPanel);
+                tma_load_3d(dst, &v_map, bar(B_VFULL + s), 0, h, z);
+                tma_load_3d(dst + kPanel, &v_map, bar(B_VFULL + s), 64, h, z);
+                vlast[s] = j;
+                return true;
+            };
+            bool ok = true;
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int s = j & 1;
+                if (j >= 2 && !wait_bar(bar(B_KEMPTY + s), ((j >> 1) - 1) & 1, abort, ds)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = sbase + OFF_K + s * 3 * kPanel;
+                const int z = (int)(key0 + 128 * j);
+                bar_arrive_expect_tx(bar(B_KFULL + s), 3 * kPanel);
+                tma_load_3d(dst, &kn_map, bar(B_KFULL + s), 0, h, z);
+                tma_load_3d(dst + kPanel, &kn_map, bar(B_KFULL + s), 64, h, z);
+                tma_load_2d(dst + 2 * kPanel, &kpe_map, bar(B_KFULL + s), 0, z);
+                klast[s] = j;
+                if (j >= 1) ok = load_v(j - 1);  // V one tile behind: it is needed after the softmax
+            }
+            if (ok) load_v(n_tiles - 1);
+            // every copy issued has landed before the CTA can leave
+            int ignore = 0;
+            wait_bar(bar(B_Q), 0, &ignore, nullptr);
+            for (int s = 0; s < 2; ++s) {
+                ignore = 0;
+                if (klast[s] >= 0) wait_bar(bar(B_KFULL + s), (klast[s] >> 1) & 1, &ignore, nullptr);
+                ignore = 0;
+                if (vlast[s] >= 0) wait_bar(bar(B_VFULL + s), (vlast[s] >> 1) & 1, &ignore, nullptr);
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = wait_bar(bar(B_Q), 0, abort, ds);
+            auto issue_pv = [&](int i) -> bool {
+                const int vs = i & 1, sb = i % 3;
+                if (!wait_bar(bar(B_VFULL + vs), (i >> 1) & 1, abort, ds)) return false;
+                if (!wait_bar(bar(B_PREADY + sb), (i / 3) & 1, abort, ds)) return false;
+                tc_fence_after();
+                const uint32_t vb = sbase + OFF_V + vs * 2 * kPanel;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // 16 keys per step: 16 rows of V, 8 columns of P
+                    mma_ts(tmem + kOCol, tmem + 128u * sb + 8u * kk, smem_desc_sw128(vb + kk * 2048, kPanel, 1024),
+                           kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(B_VEMPTY + vs));
+                mma_commit(bar(B_PVDONE + sb));
+                return true;
+            };
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int ks = j & 1, sb = j % 3;
+                if (!(ok = wait_bar(bar(B_KFULL + ks), (j >> 1) & 1, abort, ds))) break;
+                // S buffer sb last held P_{j-3}: its PV must be done before QK_j overwrites it
+                if (j >= 3 && !(ok = wait_bar(bar(B_PVDONE + sb), ((j - 3) / 3) & 1, abort, ds))) break;
+                tc_fence_after();
+                const uint32_t kb = sbase + OFF_K + ks * 3 * kPanel;
+#pragma unroll
+                for (int pn = 0; pn < 3; ++pn)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(tmem + 128u * sb, smem_desc_sw128(sbase + OFF_Q + pn * kPanel + kk * 32, 16, 1024),
+                               smem_desc_sw128(kb + pn * kPanel + kk * 32, 16, 1024), kIdescQK, (pn | kk) ? 1u : 0u);
+                mma_commit(bar(B_KEMPTY + ks));
+                mma_commit(bar(B_SFULL + sb));
+                if (j >= 1) ok = issue_pv(j - 1);
+            }
+            if (ok) issue_pv(n_tiles - 1);
+            mma_commit(bar(B_FINAL));  // lands when every MMA issued above has completed
+            int ignore = 0;
+            wait_bar(bar(B_FINAL), 0, &ignore, nullptr);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax (warps 0-3)
+        const int row = 32 * warp + lane;  // TMEM lane = query row of the tile
+        const int t = r0 + row;            // query row within the request
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        const float sl2 = p.scale * 1.4426950408889634f;
+        const int limit = p.causal ? min(n_keys, t + 1) : n_keys;  // keys [0, limit) are visible
+        float2* const sc = reinterpret_cast<float2*>(sgen + OFF_SC);
+        // l sums P as the PV MMA sees it (bf16; with FP8 before v_scale, unrounded), lt the
+        // unrounded P for the LSE; both relative to the running max m.
+        float m = -CUDART_INF_F, l = 0.f, lt = 0.f;
+        bool alive = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int sb = j % 3;
+            if (kFp8) {  // the tile's key scales, staged once for the four warps
+                const int kr = 128 * j + row;
+                sc[(j & 1) * 128 + row] = kr < n_keys ? p.scales[key0 + kr] : make_float2(0.f, 0.f);
+                named_bar(kBarScales, 128);
+            }
+            alive = alive && warp_wait(bar(B_SFULL + sb), (j / 3) & 1, abort, ds);
+            if (!alive) continue;
+            tc_fence_after();
+            uint32_t s[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + 128u * sb + 32u * c, s[c]);
+            tmem_wait_ld();
+            float mt = -CUDART_INF_F;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int k = 32 * c + i;
+                    float x = __uint_as_float(s[c][i]) * sl2;
+                    if (kFp8) x *= sc[(j & 1) * 128 + k].x;
+                    if (128 * j + k >= limit) x = -CUDART_INF_F;
+                    s[c][i] = __float_as_uint(x);
+                    mt = fmaxf(mt, x);
+                }
+            const float m_new = fmaxf(m, mt);
+            const bool need = m_new > m + 8.f;  // also true when m is still -inf
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                // O holds P_0 .. P_{j-1} V: once PV_{j-1} is done, rescale the rows that move
+                alive = warp_wait(bar(B_PVDONE + (j - 1) % 3), ((j - 1) / 3) & 1, abort, ds);
+                if (!alive) continue;
+                tc_fence_after();
+                const float f = need ? fast_exp2(m - m_new) : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_base + kOCol + 32u * c, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+                    tmem_st32(tmem + lane_base + kOCol + 32u * c, o);
+                }
+                tmem_wait_st();
+            }
+            if (need) {
+                const float f = fast_exp2(m - m_new);  // 0 while m is -inf
+                l *= f;
+                lt *= f;
+                m = m_new;
+            }
+            const float mu = m == -CUDART_INF_F ? 0.f : m;  // a row with nothing visible yet
+            uint32_t pk[2][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const int k = 32 * c + i;
+                    const float p0 = fast_exp2(__uint_as_float(s[c][i]) - mu);
+                    const float p1 = fast_exp2(__uint_as_float(s[c][i + 1]) - mu);
+                    lt += p0 + p1;
+                    uint32_t w;
+                    if (kFp8) {
+                        w = pack_bf16x2(p0 * sc[(j & 1) * 128 + k].y, p1 * sc[(j & 1) * 128 + k + 1].y);
+                        l += p0 + p1;
+                    } else {
+                        w = pack_bf16x2(p0, p1);
+                        l += bf16_lo_f(w) + bf16_hi_f(w);
+                    }
+                    pk[k >> 6][(k & 63) >> 1] = w;
+                }
+            tmem_st32(tmem + lane_base + 128u * sb, pk[0]);
+            tmem_st32(tmem + lane_base + 128u * sb + 32u, pk[1]);
+            tmem_wait_st();
+            tc_fence_before();
+            bar_arrive(bar(B_PREADY + sb));
+        }
+        // ------------------------------------------------------------ epilogue
+        const bool ok = alive && warp_wait(bar(B_PVDONE + (n_tiles - 1) % 3), ((n_tiles - 1) / 3) & 1, abort, ds);
+        float o[128];
+        if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + kOCol + 32u * c, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[32 * c + i] = __uint_as_float(r[i]);
+            }
+        }
+        if (t < q_len) {
+            const int64_t gi = (int64_t)(q_begin + t) * p.H + h;
+            float4* const od = reinterpret_cast<float4*>(p.o + gi * kV);
+            const float nan = __uint_as_float(0x7fc00000u);  // marks a CTA that gave up
+            const float inv = ok ? 1.f / l : nan;
+            float lse = ok ? (m + log2f(lt)) * 0.6931471805599453f : nan;
+            float wo = 0.f, wn = 1.f;
+            if (p.merge) {  // merge_attn_states with the earlier segments' (o, lse)
+                const float lo = p.lse[gi];
+                const float M = fmaxf(lo, lse);
+                wo = lo == -CUDART_INF_F ? 0.f : expf(lo - M);
+                wn = lse == -CUDART_INF_F ? 0.f : expf(lse - M);
+                const float ws = wo + wn;
+                lse = M + logf(ws);
+                wo /= ws;
+                wn /= ws;
+            }
+            const float fn = wn * inv;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                float4 v = make_float4(o[4 * c] * fn, o[4 * c + 1] * fn, o[4 * c + 2] * fn, o[4 * c + 3] * fn);
+                if (p.merge) {
+                    const float4 u = od[c];
+                    v.x = fmaf(wo, u.x, v.x);
+                    v.y = fmaf(wo, u.y, v.y);
+                    v.z = fmaf(wo, u.z, v.z);
+                    v.w = fmaf(wo, u.w, v.w);
+                }
+                od[c] = v;
+            }
+            p.lse[gi] = lse;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_cu_ctx(const int32_t* ctx_lens, int B, int32_t* cu_ctx, int32_t* dev_status,
+                                  cudaStream_t s) {
+    return launch_pdl(cu_ctx_kernel, dim3(1), dim3(kScanThreads), 0, s, ctx_lens, B, (int32_t)0x7fffffff, cu_ctx,
+                      dev_status);
+}
+
+cudaError_t launch_prefill_gather(const PrefillGather& g, cudaStream_t s) {
+    if (g.rows <= 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((g.rows + kGatherWarps - 1) / kGatherWarps);
+    return launch_pdl(gather_kernel, dim3(blocks), dim3(kGatherWarps * 32), 0, s, g);
+}
+
+cudaError_t launch_prefill_attn(const PrefillAttn& a, cudaStream_t s) {
+    if (a.T <= 0 || a.key_rows <= 0 || a.max_q_len <= 0) return cudaSuccess;
+    CUtensorMap qm, knm, kpm, vm;
+    cudaError_t e;
+    {
+        const uint64_t dims[3] = {192, (uint64_t)a.H, (uint64_t)a.T};
+        const uint64_t strides[2] = {192 * 2, (uint64_t)a.H * 192 * 2};
+        const uint32_t box[3] = {64, 1, 128};
+        if ((e = encode_tmap(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dims, strides, box, true)) != cudaSuccess)
+            return e;
+    }
+    {
+        const uint64_t dims[3] = {128, (uint64_t)a.H, (uint64_t)a.key_rows};
+        const uint64_t strides[2] = {128 * 2, (uint64_t)a.H * 128 * 2};
+        const uint32_t box[3] = {64, 1, 128};
+        if ((e = encode_tmap(&knm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.kn, dims, strides, box, true)) != cudaSuccess)
+            return e;
+        if ((e = encode_tmap(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v, dims, strides, box, true)) != cudaSuccess)
+            return e;
+    }
+    {
+        const uint64_t dims[2] = {64, (uint64_t)a.key_rows};
+        const uint64_t strides[1] = {64 * 2};
+        const uint32_t box[2] = {64, 128};
+        if ((e = encode_tmap(&kpm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.kpe, dims, strides, box, true)) != cudaSuccess)
+            return e;
+    }
+    const dim3 grid((unsigned)((a.max_q_len + 127) / 128), (unsigned)a.B, (unsigned)a.H);
+    if (a.scales != nullptr) {
+        if ((e = cudaFuncSetAttribute(attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem)) !=
+            cudaSuccess)
+            return e;
+        return launch_pdl(attn_kernel<true>, grid, dim3(kAttnThreads), (size_t)kAttnSmem, s, qm, knm, kpm, vm, a);
+    }
+    if ((e = cudaFuncSetAttribute(attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem)) !=
+        cudaSuccess)
+        return e;
+    return launch_pdl(attn_kernel<false>, grid, dim3(kAttnThreads), (size_t)kAttnSmem, s, qm, knm, kpm, vm, a);
+}
+
+}  // namespace mla

@@ -114,3 +114,55 @@ def test_workspace_bytes_by_cache_format(lib):
     assert mla.workspace_bytes(B, Sq, H, S, mla.KV_FP8, L) == fp8
     assert mla.workspace_bytes(B, Sq, H, 1, mla.KV_FP8, L) == up(rows * 1152) + up(rows * 8)
     assert lib.mla_decode_workspace_bytes_kv(7, B, Sq, H, S, L) == 0
+
+
+# ----------------------------------------------------------------------------- prefill host logic
+@pytest.mark.parametrize("budget", [64, 100, 128, 500, 4096, 1 << 20])
+def test_prefill_chunk_plan_is_bit_exact_with_oracle(lib, budget):
+    import numpy as np
+    rng = np.random.default_rng(budget)
+    ctx = rng.integers(0, 2000, size=57).astype(np.int32)
+    ctx[[0, 9, 10]] = 0
+    ctx[3] = 64
+    ctx[4] = 65
+    got = mla.prefill_chunk_plan(ctx, budget)
+    want = oracle.prefill_chunks(ctx, budget)
+    assert got.dtype == want.dtype and np.array_equal(got, want)
+
+
+def test_prefill_plan_and_workspace_argument_checks(lib):
+    import numpy as np
+    with pytest.raises(mla.MlaError):
+        mla.prefill_chunk_plan([10, 20], 63)
+    assert mla.prefill_workspace_bytes(4, 100, 128, 63) == 0
+    assert mla.prefill_workspace_bytes(4, 100, 129, 8192) == 0
+    ws = mla.prefill_workspace_bytes(4, 100, 128, 8192)
+    # the per-row K / V workspace dominates: 8192 rows x 128 heads x (128 + 128) bf16
+    assert ws >= 8192 * 128 * 256 * 2 and ws % 256 == 0
+    assert mla.prefill_workspace_bytes(4, 10000, 16, 64) > mla.prefill_workspace_bytes(4, 100, 16, 64)
+    assert int(lib.mla_prefill_chunk_plan(np.zeros(3, np.int32).ctypes.data, 3, 64, None, 0)) == 0
+
+
+def test_prefill_rejects_bad_arguments_before_any_launch(lib):
+    import numpy as np
+    ctx = np.array([10, 0], np.int32)
+    qsl = np.array([0, 3, 5], np.int32)
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+
+    def call(B=2, H=4, ctx_h=ctx, qsl_h=qsl, chunk=64, scale=0.07, kv=0, ws_bytes=1 << 30, max_blocks=1):
+        return int(lib.mla_prefill(fake, fake, 512, fake, 64, fake, kv, 10, fake, max_blocks, fake, fake,
+                                   ctx_h.ctypes.data, qsl_h.ctypes.data, B, H, fake, fake, scale, chunk, fake,
+                                   ws_bytes, fake, None, None, None))
+    assert call(H=0) == mla.ERR_UNSUPPORTED
+    assert call(H=129) == mla.ERR_UNSUPPORTED
+    assert call(B=0) == mla.ERR_INVALID_ARG
+    assert call(chunk=32) == mla.ERR_INVALID_ARG
+    assert call(scale=0.0) == mla.ERR_INVALID_ARG
+    assert call(kv=5) == mla.ERR_INVALID_ARG
+    assert call(qsl_h=np.array([1, 3, 5], np.int32)) == mla.ERR_INVALID_ARG
+    assert call(qsl_h=np.array([0, 3, 2], np.int32)) == mla.ERR_INVALID_ARG
+    assert call(ctx_h=np.array([65, 0], np.int32), max_blocks=1) == mla.ERR_INVALID_ARG
+    assert call(ctx_h=np.array([-1, 0], np.int32)) == mla.ERR_INVALID_ARG
+    assert call(ws_bytes=100) == mla.ERR_WORKSPACE_TOO_SMALL
+    # nothing to do: no query rows
+    assert call(qsl_h=np.array([0, 0, 0], np.int32)) == mla.OK
