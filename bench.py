@@ -44,9 +44,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dsv3", choices=sorted(mi.WORKLOADS))
-    ap.add_argument("--component", default="step", choices=["step", "cache_write"],
+    ap.add_argument("--component", default="step", choices=["step", "cache_write", "prefill"],
                     help="step: absorb -> decode -> out_proj (the hot path); cache_write: the KV cache "
-                         "write that precedes it, measured alone (FP8 quantise for the fp8 workload)")
+                         "write that precedes it, measured alone (FP8 quantise for the fp8 workload); "
+                         "prefill: the compute-friendly prefill route on a DeepSeek-V3-shaped batch")
     ap.add_argument("--num-splits", type=int, default=-1,
                     help="-1: GB300 planner, 0: the pages' Triton rule, >0 forced")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline sample budget")
@@ -457,12 +458,98 @@ def run_cache_write(args):
     print(json.dumps(line), flush=True)
 
 
+PREFILL = dict(ctx=4096, q=1024, B=4, H=128, chunk_rows=8192)
+
+
+def prefill_flops(ctx, ql, H):
+    """Algorithmic flops of the prefill route: the up-projection of every gathered and new row
+    (512 -> 128 + 128 per head) and the attention over each query's visible keys (192-dim q.k,
+    128-dim p.v per head)."""
+    ctx, ql = np.asarray(ctx, np.int64), np.asarray(ql, np.int64)
+    rows = int(ctx.sum() + ql.sum())
+    pairs = int((ql * ctx + ql * (ql + 1) // 2).sum())
+    up = rows * H * 2 * 512 * 256
+    attn = pairs * H * 2 * (192 + 128)
+    return up + attn, up, attn
+
+
+def run_prefill(args):
+    """mla_prefill on a DeepSeek-V3-shaped chunked-prefill batch: B requests, each with `ctx`
+    cached tokens and `q` new ones, H = 128, bf16 cache (FP8 for the fp8 workload). Tensor-bound:
+    roofline against the dense bf16 peak, counting the route's algorithmic flops."""
+    import torch
+    import mla_latent_kv_gb300 as mla
+    mla.lib()
+    dev = torch.device("cuda", 0)
+    kv = mi.WORKLOADS[args.workload]["kv"]
+    w = PREFILL
+    B, H = w["B"], w["H"]
+    c = mi.prefill_case([w["ctx"]] * B, [w["q"]] * B, H, kv=kv, seed=31, poison=False)
+    d16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa
+    q, kv_c, k_pe = d16(c["q"]), d16(c["kv_c_new"]), d16(c["k_pe_new"])
+    wk, wv = d16(c["w_uk_t"]), d16(c["w_uv"])
+    cache = torch.from_numpy(c["cache"]).to(dev)
+    bt = torch.from_numpy(c["block_table"]).to(dev)
+    ctx_d = torch.from_numpy(c["ctx_lens"]).to(dev)
+    qsl_d = torch.from_numpy(c["query_start_loc"]).to(dev)
+    ctx_h = torch.from_numpy(c["ctx_lens"].copy())
+    qsl_h = torch.from_numpy(c["query_start_loc"].copy())
+    T = int(c["query_start_loc"][-1])
+    ws = torch.empty(mla.prefill_workspace_bytes(B, T, H, w["chunk_rows"]), dtype=torch.uint8, device=dev)
+    o = torch.empty((T, H, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(args.flush_mb * (1 << 20), dtype=torch.uint8, device=dev)
+
+    def call():
+        mla.prefill(q, kv_c, k_pe, cache, bt, ctx_d, qsl_d, wk, wv, c["scale"], kv_dtype=kv,
+                    chunk_rows=w["chunk_rows"], workspace=ws, o=o, lse=lse, dev_status=status,
+                    num_blocks=c["num_blocks"], ctx_lens_host=ctx_h, query_start_loc_host=qsl_h)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(None)
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    assert int(status.item()) == 0
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    flops, up, attn = prefill_flops(c["ctx_lens"], np.diff(c["query_start_loc"]), H)
+    n_chunks = int(mla.prefill_chunk_plan(c["ctx_lens"], w["chunk_rows"])[:, 0].max()) + 1
+    launches = 1 + 4 * (1 + n_chunks)
+    peaks, src = load_peaks()
+    tf = flops / (ms * 1e-3) / 1e12
+    line = {"metric": "MLA prefill new tokens/s (compute-friendly route)", "value": T / (ms * 1e-3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"prefill: B={B} requests x {w['q']} new tokens over {w['ctx']} cached tokens, "
+                                   f"H={H}, {'FP8' if kv else 'bf16'} cache, chunk_rows={w['chunk_rows']}",
+                       "l2": f"{args.flush_mb} MB L2 flush between calls", "chunks": n_chunks},
+            "prefill_tflops": tf,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"], "traffic": None,
+                         "kernel": "mla_prefill (gather, up-projection GEMMs, attention; whole call)",
+                         "flops_per_launch": flops, "flops_up_projection": up, "flops_attention": attn,
+                         "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json)"},
+            "gpu_launches": launches * K, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
     elif args.component == "cache_write":
         run_cache_write(args)
+    elif args.component == "prefill":
+        run_prefill(args)
     else:
         run_ours(args)
 

@@ -274,17 +274,19 @@ def prefill_chunk_plan(ctx_lens, chunk_rows):
 
 def prefill(q, kv_c, k_pe, kv_cache, block_table, ctx_lens, query_start_loc, w_uk_t, w_uv, scale,
             kv_dtype=KV_BF16, chunk_rows=8192, workspace=None, o=None, lse=None, dev_status=None, stream=None,
-            num_blocks=None):
+            num_blocks=None, ctx_lens_host=None, query_start_loc_host=None):
     """Prefill through the compute-friendly route. q [total_q, H, 192] bf16 (q_nope || q_pe),
     kv_c [total_q, 512] / k_pe [total_q, 64] bf16 (the new tokens' rows, row-strided allowed),
     ctx_lens [B] and query_start_loc [B + 1] int32 device tensors (read once on the host for the
-    launch plan) -> (o [total_q, H, 128] fp32, lse [total_q, H] fp32)."""
+    launch plan, unless host copies are passed as ctx_lens_host / query_start_loc_host int32 CPU
+    tensors) -> (o [total_q, H, 128] fp32, lse [total_q, H] fp32)."""
     import torch
     total_q, H = q.shape[0], q.shape[1]
     B = int(query_start_loc.shape[0]) - 1
     dev = q.device
-    ctx_host = ctx_lens.to("cpu", torch.int32).contiguous()
-    qsl_host = query_start_loc.to("cpu", torch.int32).contiguous()
+    ctx_host = ctx_lens.to("cpu", torch.int32).contiguous() if ctx_lens_host is None else ctx_lens_host
+    qsl_host = query_start_loc.to("cpu", torch.int32).contiguous() if query_start_loc_host is None \
+        else query_start_loc_host
     if num_blocks is None:
         num_blocks = kv_cache.numel() * kv_cache.element_size() // (PAGE * row_bytes(kv_dtype))
     need = prefill_workspace_bytes(B, total_q, H, chunk_rows)

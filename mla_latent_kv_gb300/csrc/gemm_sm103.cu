@@ -71,6 +71,7 @@ struct HeadGemmArgs {
     int64_t pe_st, pe_sh;
     int x_shared;            // one activation row per token, used by every head (up_proj)
     int w_kmajor;            // weights stored [H][M][K] (k fastest) instead of [H][K][M]
+    int64_t out_m_ext;       // extent of the output's m dimension (0: out_sh, m runs up to the head stride)
 };
 
 struct Unit {
@@ -410,7 +411,7 @@ cudaError_t launch_head_gemm(HeadGemmArgs a, const uint16_t* w, const void* x, i
     {
         const uint64_t es = a.out_f32 ? 4 : 2;
         const int64_t ost = a.T == 1 ? a.out_sh * a.H : a.out_st;
-        const uint64_t dims[3] = {(uint64_t)a.out_sh, (uint64_t)a.H, (uint64_t)a.T};
+        const uint64_t dims[3] = {(uint64_t)(a.out_m_ext > 0 ? a.out_m_ext : a.out_sh), (uint64_t)a.H, (uint64_t)a.T};
         const uint64_t strides[2] = {(uint64_t)a.out_sh * es, (uint64_t)ost * es};
         const uint32_t box[3] = {128u, 1u, (uint32_t)kSlice};
         cudaError_t e = encode_tmap(&omap, a.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -478,9 +479,9 @@ cudaError_t launch_out_proj_sm103(const void* o_latent, int in_dtype, const uint
     return launch_head_gemm(a, w_uv, o_latent, (int64_t)H * kL, kL, s);
 }
 
-// Up-projection of gathered latent rows: out[j, h, m] = sum_l x[j, l] * W[h] with W_UK_T[h]
+// Up-projection of gathered latent rows: out[h, j, m] = sum_l x[j, l] * W[h] with W_UK_T[h]
 // ([H][128][512], K-major) for k_nope or W_UV[h] ([H][512][128]) for v; x [rows, 512] bf16
-// with row stride x_st; out [rows, H, 128] bf16.
+// with row stride x_st; out [H, rows, 128] bf16 (head-major: one head's rows are contiguous).
 cudaError_t launch_up_proj_sm103(const uint16_t* x, int64_t x_st, int rows, const uint16_t* w, bool w_is_uk,
                                  uint16_t* out, int H, cudaStream_t s) {
     HeadGemmArgs a{};
@@ -493,8 +494,9 @@ cudaError_t launch_up_proj_sm103(const uint16_t* x, int64_t x_st, int rows, cons
     a.x_f32 = 0;
     a.out = out;
     a.out_f32 = 0;
-    a.out_st = (int64_t)H * 128;
-    a.out_sh = 128;
+    a.out_st = 128;
+    a.out_sh = (int64_t)rows * 128;
+    a.out_m_ext = 128;
     a.q_pe = nullptr;
     a.x_shared = 1;
     a.w_kmajor = w_is_uk ? 1 : 0;

@@ -181,8 +181,8 @@ struct PrefillGather {
 // result is written (merge = 0) or merged by LSE into o / lse (merge = 1).
 struct PrefillAttn {
     const uint16_t* q;          // [T, H, 192]
-    const uint16_t* kn;         // [key_rows, H, 128] up-projected k_nope
-    const uint16_t* v;          // [key_rows, H, 128] up-projected v
+    const uint16_t* kn;         // [H, key_rows, 128] up-projected k_nope (head-major)
+    const uint16_t* v;          // [H, key_rows, 128] up-projected v (head-major)
     const uint16_t* kpe;        // [key_rows, 64]
     const float2* scales;       // FP8 only: per key row (k_scale, v_scale)
     int key_rows;

@@ -10,20 +10,22 @@
 //   2. the context, in chunks of at most chunk_rows gathered rows; each chunk's result is merged
 //      into the running one by LSE in the attention kernel's epilogue (merge_attn_states).
 //
-// Attention kernel: one CTA per (128-query tile, request, head), 192 threads, 1 CTA per SM.
-//   warp 4 lane 0   TMA: the q tile (three 64-dim panels); per 128-key tile the K panels
-//                   (k_nope dims 0-63 and 64-127 of this head, k_pe shared by all heads) into a
-//                   2-stage ring and, one tile behind, the two V panels into another 2-stage ring
-//   warp 5 lane 0   tcgen05.mma: S_j = Q K_j^T (M = 128 queries, N = 128 keys, K = 192) into one
-//                   of three 128-column TMEM buffers, then O += P_{j-1} V_{j-1} with P read from
-//                   TMEM (M = 128, N = 128 dims, K = 128 keys; V is an MN-major operand)
-//   warps 0-3       softmax, one query row per thread (its TMEM lane): fp32 online softmax in the
-//                   exp2 domain with a lazily moved running max (O and l are rescaled only when a
-//                   row's max grows by more than 2^8); P goes back over S as bf16; at the end
-//                   O / l and the LSE, merged with the result of the earlier segments
+// Attention kernel: one CTA per (128-query tile, request, head), 320 threads, 1 CTA per SM.
+//   warp 8 lane 0   TMA: the q tile (three 64-dim panels); per 128-key tile the K panels (k_nope dims 0-63 and 64-127 of this head,
+//                   k_pe shared by all heads) into a 2-stage ring and, one tile behind, the two
+//                   V panels into another 2-stage ring
+//   warp 9 lane 0   tcgen05.mma: S_j = Q K_j^T (M = 128 queries, N = 128 keys, K = 192, both
+//                   operands in shared memory) into one of three 128-column TMEM buffers, one key
+//                   tile ahead of O += P_{j-1} V_{j-1} (P read from TMEM over S, V an MN-major
+//                   operand in shared memory)
+//   warps 0-7       softmax, two warps per TMEM lane quarter (one query row per lane, 64 key
+//                   columns per warp): fp32 online softmax in the exp2 domain with a lazily moved
+//                   running max (O and l are rescaled only when a row's max grows by more than
+//                   2^8); P goes back over S as bf16; at the end O / l and the LSE, merged with
+//                   the result of the earlier segments
 // FP8 cache: the gathered rows hold the e4m3 values unscaled; k_scale multiplies the key's logit
 // column and v_scale its P column, which is exact because the up-projection is linear.
-// TMEM: S buffers at columns 0, 128, 256; O at 384..511. Every wait is bounded.
+// TMEM: S buffers at columns 0, 128 and 256, O at 384..511. Every wait is bounded.
 #include <cuda.h>
 #include <math_constants.h>
 
@@ -150,25 +152,29 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(PrefillGather
 }
 
 // ---------------------------------------------------------------- attention
-constexpr int kAttnThreads = 192;        // warps 0-3 softmax, 4 TMA + TMEM, 5 MMA
-constexpr int kPanel = 128 * 128;        // 128 rows x 64 bf16 with the 128-byte swizzle: 16 KB
-constexpr int OFF_Q = 0;                 // 3 panels
-constexpr int OFF_K = 3 * kPanel;        // 2 stages x 3 panels
-constexpr int OFF_V = 9 * kPanel;        // 2 stages x 2 panels
-constexpr int OFF_SC = 13 * kPanel;      // FP8: 2 x 128 (k_scale, v_scale)
-constexpr int kAttnSmem = OFF_SC + 2 * 128 * 8 + 1024;  // + 1024-byte alignment slack
+constexpr int kAttnThreads = 320;       // warps 0-7 softmax, 8 TMA + TMEM, 9 MMA
+constexpr int kPanel = 128 * 128;       // 128 rows x 64 bf16 (128-byte swizzle): 16 KB
+constexpr int OFF_Q = 0;                // 3 panels (the A operand of QK)
+constexpr int OFF_K = 3 * kPanel;       // 2 stages x 3 panels (k_nope 0-63, 64-127, k_pe)
+constexpr int OFF_V = 9 * kPanel;       // 2 stages x 2 panels
+constexpr int OFF_SC = 13 * kPanel;     // FP8: 2 x 128 (k_scale, v_scale)
+// row maxima of the two column halves per tile parity (2 x 2 x 128), then the row sums (2 x 128)
+constexpr int OFF_MX = OFF_SC + 2 * 128 * 8;
+constexpr int kAttnSmem = OFF_MX + 6 * 128 * 4 + 1024;  // + 1024-byte alignment slack
+constexpr int kSBufs = 3;               // TMEM: S buffers at 0, 128, 256; O at 384
 constexpr uint32_t kOCol = 384;
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
-constexpr uint32_t kBarScales = 1;       // named barrier of the softmax warps
+constexpr uint32_t kBarScales = 1;      // named barrier of the eight softmax warps
+constexpr uint32_t kBarPair0 = 2;       // 2 + q: the two softmax warps of TMEM lane quarter q
 enum {
-    B_Q = 0,
+    B_Q = 0,        // q tile landed in shared memory
     B_KFULL = 1,    // 2
     B_KEMPTY = 3,   // 2
     B_VFULL = 5,    // 2
     B_VEMPTY = 7,   // 2
     B_SFULL = 9,    // 3
-    B_PREADY = 12,  // 3
+    B_PREADY = 12,  // 3 (256 arrivals)
     B_PVDONE = 15,  // 3
     B_FINAL = 18,
     kNumBars = 19
@@ -227,15 +233,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             bar_init(bar(B_VFULL + i), 1);
             bar_init(bar(B_VEMPTY + i), 1);
         }
-        for (int i = 0; i < 3; ++i) {
+        for (int i = 0; i < kSBufs; ++i) {
             bar_init(bar(B_SFULL + i), 1);
-            bar_init(bar(B_PREADY + i), 128);
+            bar_init(bar(B_PREADY + i), 256);
             bar_init(bar(B_PVDONE + i), 1);
         }
         bar_init(bar(B_FINAL), 1);
         fence_barrier_init();
     }
-    if (warp == 4) {
+    if (warp == 8) {
         tmem_alloc(smem_addr(&tmem_slot), 512);
         tmem_relinquish();
     }
@@ -245,7 +251,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t tmem = tmem_slot;
     volatile int* abort = &abort_flag;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&q_map);
@@ -257,223 +263,286 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 tma_load_3d(sbase + OFF_Q + pn * kPanel, &q_map, bar(B_Q), 64 * pn, h, q_begin + r0);
             int klast[2] = {-1, -1}, vlast[2] = {-1, -1};
             auto load_v = [&](int j) -> bool {
-                const int s = j & 1;
-                if (j >= 2 && !wait_bar(bar(B_VEMPTY + s), ((j >> 1) - 1) & 1, abort, ds)) return false;
-                const uint32_t dst = sbase + OFF_V + s * 2 * kPanel;
+                const int st = j & 1;
+                if (j >= 2 && !wait_bar(bar(B_VEMPTY + st), ((j >> 1) - 1) & 1, abort, ds)) return false;
+                const uint32_t dst = sbase + OFF_V + st * 2 * kPanel;
                 const int z = (int)(key0 + 128 * j);
-                bar_arrive_expect_tx(bar(B_VFULL + s), 2 * kPanel);
-                tma_load_3d(dst, &v_map, bar(B_VFULL + s), 0, h, z);
-                tma_load_3d(dst + kPanel, &v_map, bar(B_VFULL + s), 64, h, z);
-                vlast[s] = j;
+                bar_arrive_expect_tx(bar(B_VFULL + st), 2 * kPanel);
+                tma_load_3d(dst, &v_map, bar(B_VFULL + st), 0, z, h);
+                tma_load_3d(dst + kPanel, &v_map, bar(B_VFULL + st), 64, z, h);
+                vlast[st] = j;
                 return true;
             };
             bool ok = true;
             for (int j = 0; j < n_tiles && ok; ++j) {
-                const int s = j & 1;
-                if (j >= 2 && !wait_bar(bar(B_KEMPTY + s), ((j >> 1) - 1) & 1, abort, ds)) {
+                const int st = j & 1;
+                if (j >= 2 && !wait_bar(bar(B_KEMPTY + st), ((j >> 1) - 1) & 1, abort, ds)) {
                     ok = false;
                     break;
                 }
-                const uint32_t dst = sbase + OFF_K + s * 3 * kPanel;
+                const uint32_t dst = sbase + OFF_K + st * 3 * kPanel;
                 const int z = (int)(key0 + 128 * j);
-                bar_arrive_expect_tx(bar(B_KFULL + s), 3 * kPanel);
-                tma_load_3d(dst, &kn_map, bar(B_KFULL + s), 0, h, z);
-                tma_load_3d(dst + kPanel, &kn_map, bar(B_KFULL + s), 64, h, z);
-                tma_load_2d(dst + 2 * kPanel, &kpe_map, bar(B_KFULL + s), 0, z);
-                klast[s] = j;
+                bar_arrive_expect_tx(bar(B_KFULL + st), 3 * kPanel);
+                tma_load_3d(dst, &kn_map, bar(B_KFULL + st), 0, z, h);
+                tma_load_3d(dst + kPanel, &kn_map, bar(B_KFULL + st), 64, z, h);
+                tma_load_2d(dst + 2 * kPanel, &kpe_map, bar(B_KFULL + st), 0, z);
+                klast[st] = j;
                 if (j >= 1) ok = load_v(j - 1);  // V one tile behind: it is needed after the softmax
             }
             if (ok) load_v(n_tiles - 1);
             // every copy issued has landed before the CTA can leave
             int ignore = 0;
             wait_bar(bar(B_Q), 0, &ignore, nullptr);
-            for (int s = 0; s < 2; ++s) {
+            for (int st = 0; st < 2; ++st) {
                 ignore = 0;
-                if (klast[s] >= 0) wait_bar(bar(B_KFULL + s), (klast[s] >> 1) & 1, &ignore, nullptr);
+                if (klast[st] >= 0) wait_bar(bar(B_KFULL + st), (klast[st] >> 1) & 1, &ignore, nullptr);
                 ignore = 0;
-                if (vlast[s] >= 0) wait_bar(bar(B_VFULL + s), (vlast[s] >> 1) & 1, &ignore, nullptr);
+                if (vlast[st] >= 0) wait_bar(bar(B_VFULL + st), (vlast[st] >> 1) & 1, &ignore, nullptr);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
+        // QK runs one key tile ahead of PV: QK(j + 1) is issued before PV(j), so the softmax of
+        // tile j overlaps it. With three S buffers, QK(j + 1) reuses the buffer of tile j - 2,
+        // whose PV was issued a whole step earlier, so the wait for it does not drain the pipe.
         if (lane == 0) {
             bool ok = wait_bar(bar(B_Q), 0, abort, ds);
-            auto issue_pv = [&](int i) -> bool {
-                const int vs = i & 1, sb = i % 3;
-                if (!wait_bar(bar(B_VFULL + vs), (i >> 1) & 1, abort, ds)) return false;
-                if (!wait_bar(bar(B_PREADY + sb), (i / 3) & 1, abort, ds)) return false;
+            auto issue_qk = [&](int j) -> bool {
+                const int st = j & 1, sb = j % kSBufs;
+                if (!wait_bar(bar(B_KFULL + st), (j >> 1) & 1, abort, ds)) return false;
+                if (j >= kSBufs && !wait_bar(bar(B_PVDONE + sb), ((j - kSBufs) / kSBufs) & 1, abort, ds)) return false;
                 tc_fence_after();
-                const uint32_t vb = sbase + OFF_V + vs * 2 * kPanel;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // 16 keys per step: 16 rows of V, 8 columns of P
-                    mma_ts(tmem + kOCol, tmem + 128u * sb + 8u * kk, smem_desc_sw128(vb + kk * 2048, kPanel, 1024),
-                           kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar(B_VEMPTY + vs));
-                mma_commit(bar(B_PVDONE + sb));
-                return true;
-            };
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                const int ks = j & 1, sb = j % 3;
-                if (!(ok = wait_bar(bar(B_KFULL + ks), (j >> 1) & 1, abort, ds))) break;
-                // S buffer sb last held P_{j-3}: its PV must be done before QK_j overwrites it
-                if (j >= 3 && !(ok = wait_bar(bar(B_PVDONE + sb), ((j - 3) / 3) & 1, abort, ds))) break;
-                tc_fence_after();
-                const uint32_t kb = sbase + OFF_K + ks * 3 * kPanel;
+                const uint32_t kb = sbase + OFF_K + st * 3 * kPanel;
 #pragma unroll
                 for (int pn = 0; pn < 3; ++pn)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         mma_ss(tmem + 128u * sb, smem_desc_sw128(sbase + OFF_Q + pn * kPanel + kk * 32, 16, 1024),
                                smem_desc_sw128(kb + pn * kPanel + kk * 32, 16, 1024), kIdescQK, (pn | kk) ? 1u : 0u);
-                mma_commit(bar(B_KEMPTY + ks));
+                mma_commit(bar(B_KEMPTY + st));
                 mma_commit(bar(B_SFULL + sb));
-                if (j >= 1) ok = issue_pv(j - 1);
+                return true;
+            };
+            auto issue_pv = [&](int i) -> bool {
+                const int st = i & 1, sb = i % kSBufs;
+                if (!wait_bar(bar(B_VFULL + st), (i >> 1) & 1, abort, ds)) return false;
+                if (!wait_bar(bar(B_PREADY + sb), (i / kSBufs) & 1, abort, ds)) return false;
+                tc_fence_after();
+                const uint32_t vb = sbase + OFF_V + st * 2 * kPanel;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // 16 keys per step: 16 rows of V, 8 columns of P
+                    mma_ts(tmem + kOCol, tmem + 128u * sb + 8u * kk, smem_desc_sw128(vb + kk * 2048, kPanel, 1024),
+                           kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(B_VEMPTY + st));
+                mma_commit(bar(B_PVDONE + sb));
+                return true;
+            };
+            if (ok) ok = issue_qk(0);
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                if (j + 1 < n_tiles && !(ok = issue_qk(j + 1))) break;
+                ok = issue_pv(j);
             }
-            if (ok) issue_pv(n_tiles - 1);
             mma_commit(bar(B_FINAL));  // lands when every MMA issued above has completed
             int ignore = 0;
             wait_bar(bar(B_FINAL), 0, &ignore, nullptr);
         }
     } else {
-        // ------------------------------------------------------------ softmax (warps 0-3)
-        const int row = 32 * warp + lane;  // TMEM lane = query row of the tile
-        const int t = r0 + row;            // query row within the request
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        // ------------------------------------------------------------ softmax (warps 0-7)
+        // Warp w owns TMEM lane quarter w % 4 (32 query rows) and key columns [64 hf, 64 hf + 64)
+        // of each tile, hf = w / 4; the two warps of a quarter agree on each row's max through
+        // shared memory. Every named barrier below runs on every tile whatever the waits
+        // returned, so that a wait that gives up cannot leave the partner warp stuck.
+        const int quarter = warp & 3, hf = warp >> 2;
+        const int row = 32 * quarter + lane;  // TMEM lane = query row of the tile
+        const int t = r0 + row;               // query row within the request
+        const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+        const uint32_t pair_bar = kBarPair0 + (uint32_t)quarter;
         const float sl2 = p.scale * 1.4426950408889634f;
         const int limit = p.causal ? min(n_keys, t + 1) : n_keys;  // keys [0, limit) are visible
         float2* const sc = reinterpret_cast<float2*>(sgen + OFF_SC);
-        // l sums P as the PV MMA sees it (bf16; with FP8 before v_scale, unrounded), lt the
-        // unrounded P for the LSE; both relative to the running max m.
-        float m = -CUDART_INF_F, l = 0.f, lt = 0.f;
+        float* const mx = reinterpret_cast<float*>(sgen + OFF_MX);  // [tile parity][hf][row]
+        // running max m (exp2 domain) and the sum of this half's P relative to it
+        float m = -CUDART_INF_F, lt = 0.f;
         bool alive = true;
         for (int j = 0; j < n_tiles; ++j) {
-            const int sb = j % 3;
-            if (kFp8) {  // the tile's key scales, staged once for the four warps
-                const int kr = 128 * j + row;
-                sc[(j & 1) * 128 + row] = kr < n_keys ? p.scales[key0 + kr] : make_float2(0.f, 0.f);
-                named_bar(kBarScales, 128);
-            }
-            alive = alive && warp_wait(bar(B_SFULL + sb), (j / 3) & 1, abort, ds);
-            if (!alive) continue;
-            tc_fence_after();
-            uint32_t s[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + 128u * sb + 32u * c, s[c]);
-            tmem_wait_ld();
-            float mt = -CUDART_INF_F;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int k = 32 * c + i;
-                    float x = __uint_as_float(s[c][i]) * sl2;
-                    if (kFp8) x *= sc[(j & 1) * 128 + k].x;
-                    if (128 * j + k >= limit) x = -CUDART_INF_F;
-                    s[c][i] = __float_as_uint(x);
-                    mt = fmaxf(mt, x);
+            const int sb = j % kSBufs;
+            if (kFp8) {  // the tile's key scales, staged once for the eight warps
+                if (threadIdx.x < 128) {
+                    const int kr = 128 * j + threadIdx.x;
+                    sc[(j & 1) * 128 + threadIdx.x] = kr < n_keys ? p.scales[key0 + kr] : make_float2(0.f, 0.f);
                 }
+                named_bar(kBarScales, 256);
+            }
+            const bool ok_s = alive && warp_wait(bar(B_SFULL + sb), (j / kSBufs) & 1, abort, ds);
+            uint32_t s[2][32];
+            float mt = -CUDART_INF_F;
+            const int kb = 128 * j + 64 * hf;  // first key of this warp's columns
+            if (ok_s) {
+                tc_fence_after();
+                tmem_ld32(tmem + lane_base + 128u * sb + 64u * hf, s[0]);
+                tmem_ld32(tmem + lane_base + 128u * sb + 64u * hf + 32u, s[1]);
+                tmem_wait_ld();
+                const bool masked = __any_sync(0xffffffffu, kb + 64 > limit);
+                float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+                if (kFp8) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            s[c][i] = __float_as_uint(__uint_as_float(s[c][i]) * (sl2 * sc[(j & 1) * 128 + 64 * hf + 32 * c + i].x));
+                }
+                if (masked) {  // a tile that reaches past a row's last visible key
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (kb + 32 * c + i >= limit) s[c][i] = __float_as_uint(-CUDART_INF_F);
+                }
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(s[c][i]));
+                mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                if (!kFp8) mt *= sl2;  // bf16: the scale is applied with the exponent below
+            }
+            mx[((j & 1) * 2 + hf) * 128 + row] = mt;
+            named_bar(pair_bar, 64);
+            mt = fmaxf(mt, mx[((j & 1) * 2 + (hf ^ 1)) * 128 + row]);
+            alive = ok_s;
+            if (!alive) continue;
             const float m_new = fmaxf(m, mt);
             const bool need = m_new > m + 8.f;  // also true when m is still -inf
             if (j > 0 && __any_sync(0xffffffffu, need)) {
-                // O holds P_0 .. P_{j-1} V: once PV_{j-1} is done, rescale the rows that move
-                alive = warp_wait(bar(B_PVDONE + (j - 1) % 3), ((j - 1) / 3) & 1, abort, ds);
+                // O holds P_0 .. P_{j-1} V: once PV_{j-1} is done, rescale this warp's half of
+                // the rows that move
+                alive = warp_wait(bar(B_PVDONE + (j - 1) % kSBufs), ((j - 1) / kSBufs) & 1, abort, ds);
                 if (!alive) continue;
                 tc_fence_after();
                 const float f = need ? fast_exp2(m - m_new) : 1.f;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + kOCol + 32u * c, o);
+                    const uint32_t col = tmem + lane_base + kOCol + 64u * hf + 32u * c;
+                    tmem_ld32(col, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-                    tmem_st32(tmem + lane_base + kOCol + 32u * c, o);
+                    tmem_st32(col, o);
                 }
                 tmem_wait_st();
             }
             if (need) {
-                const float f = fast_exp2(m - m_new);  // 0 while m is -inf
-                l *= f;
-                lt *= f;
+                lt *= fast_exp2(m - m_new);  // 0 while m is -inf
                 m = m_new;
             }
             const float mu = m == -CUDART_INF_F ? 0.f : m;  // a row with nothing visible yet
-            uint32_t pk[2][32];
+            uint32_t pk[32];
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const int k = 32 * c + i;
-                    const float p0 = fast_exp2(__uint_as_float(s[c][i]) - mu);
-                    const float p1 = fast_exp2(__uint_as_float(s[c][i + 1]) - mu);
-                    lt += p0 + p1;
-                    uint32_t w;
+                    float p0, p1;
                     if (kFp8) {
-                        w = pack_bf16x2(p0 * sc[(j & 1) * 128 + k].y, p1 * sc[(j & 1) * 128 + k + 1].y);
-                        l += p0 + p1;
+                        p0 = fast_exp2(__uint_as_float(s[c][i]) - mu);
+                        p1 = fast_exp2(__uint_as_float(s[c][i + 1]) - mu);
                     } else {
-                        w = pack_bf16x2(p0, p1);
-                        l += bf16_lo_f(w) + bf16_hi_f(w);
+                        p0 = fast_exp2(fmaf(__uint_as_float(s[c][i]), sl2, -mu));
+                        p1 = fast_exp2(fmaf(__uint_as_float(s[c][i + 1]), sl2, -mu));
                     }
-                    pk[k >> 6][(k & 63) >> 1] = w;
+                    l4[(i >> 1) & 3] += p0 + p1;
+                    if (kFp8) {
+                        const int k = 64 * hf + 32 * c + i;
+                        pk[16 * c + i / 2] = pack_bf16x2(p0 * sc[(j & 1) * 128 + k].y, p1 * sc[(j & 1) * 128 + k + 1].y);
+                    } else {
+                        pk[16 * c + i / 2] = pack_bf16x2(p0, p1);
+                    }
                 }
-            tmem_st32(tmem + lane_base + 128u * sb, pk[0]);
-            tmem_st32(tmem + lane_base + 128u * sb + 32u, pk[1]);
+            lt += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+            tmem_st32(tmem + lane_base + 128u * sb + 32u * hf, pk);  // P over S: keys 64 hf .. at 32 hf
             tmem_wait_st();
             tc_fence_before();
             bar_arrive(bar(B_PREADY + sb));
         }
         // ------------------------------------------------------------ epilogue
-        const bool ok = alive && warp_wait(bar(B_PVDONE + (n_tiles - 1) % 3), ((n_tiles - 1) / 3) & 1, abort, ds);
-        float o[128];
-        if (ok) {
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + kOCol + 32u * c, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[32 * c + i] = __uint_as_float(r[i]);
+        // Rows of o are 64 KB apart in global memory (one head of a token), so each warp passes its
+        // 32 rows x 64 columns through a shared-memory slab in the freed K ring and moves them
+        // with whole 256-byte rows per instruction. The earlier segments' result is read first,
+        // while the last PV is still running.
+        constexpr int kSlabStride = 68;  // floats per slab row (padding keeps 16-byte accesses conflict-free)
+        float* const slab = reinterpret_cast<float*>(sgen + OFF_K) + warp * 32 * kSlabStride;
+        const bool live_row = t < q_len;
+        const int64_t gi = (int64_t)(q_begin + (live_row ? t : 0)) * p.H + h;
+        const float lse_old = (p.merge && live_row) ? p.lse[gi] : -CUDART_INF_F;  // read before either half writes
+        const int sub = lane >> 4, c4 = lane & 15;  // coalesced phase: two rows per instruction
+        if (p.merge) {
+#pragma unroll 4
+            for (int r2 = 0; r2 < 16; ++r2) {
+                const int rl = 2 * r2 + sub, tq = r0 + 32 * quarter + rl;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tq < q_len)
+                    v = *reinterpret_cast<const float4*>(p.o + ((int64_t)(q_begin + tq) * p.H + h) * kV + 64 * hf + 4 * c4);
+                *reinterpret_cast<float4*>(slab + rl * kSlabStride + 4 * c4) = v;
             }
         }
-        if (t < q_len) {
-            const int64_t gi = (int64_t)(q_begin + t) * p.H + h;
-            float4* const od = reinterpret_cast<float4*>(p.o + gi * kV);
-            const float nan = __uint_as_float(0x7fc00000u);  // marks a CTA that gave up
-            const float inv = ok ? 1.f / l : nan;
-            float lse = ok ? (m + log2f(lt)) * 0.6931471805599453f : nan;
-            float wo = 0.f, wn = 1.f;
-            if (p.merge) {  // merge_attn_states with the earlier segments' (o, lse)
-                const float lo = p.lse[gi];
-                const float M = fmaxf(lo, lse);
-                wo = lo == -CUDART_INF_F ? 0.f : expf(lo - M);
-                wn = lse == -CUDART_INF_F ? 0.f : expf(lse - M);
-                const float ws = wo + wn;
-                lse = M + logf(ws);
-                wo /= ws;
-                wn /= ws;
-            }
-            const float fn = wn * inv;
+        const bool ok =
+            alive && warp_wait(bar(B_PVDONE + (n_tiles - 1) % kSBufs), ((n_tiles - 1) / kSBufs) & 1, abort, ds);
+        mx[(4 + hf) * 128 + row] = lt;  // the row's sum is the two halves' sums (same running max)
+        named_bar(pair_bar, 64);
+        const float l = lt + mx[(4 + (hf ^ 1)) * 128 + row];
+        const float nan = __uint_as_float(0x7fc00000u);  // marks a CTA that gave up
+        const float inv = ok ? 1.f / l : nan;
+        float lse = ok ? (m + log2f(l)) * 0.6931471805599453f : nan;
+        float wo = 0.f, wn = 1.f;
+        if (p.merge) {  // merge_attn_states with the earlier segments' (o, lse)
+            const float M = fmaxf(lse_old, lse);
+            wo = lse_old == -CUDART_INF_F ? 0.f : expf(lse_old - M);
+            wn = lse == -CUDART_INF_F ? 0.f : expf(lse - M);
+            const float ws = wo + wn;
+            lse = M + logf(ws);
+            wo /= ws;
+            wn /= ws;
+        }
+        const float fn = wn * inv;
+        if (ok) tc_fence_after();
+        __syncwarp();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                float4 v = make_float4(o[4 * c] * fn, o[4 * c + 1] * fn, o[4 * c + 2] * fn, o[4 * c + 3] * fn);
+        for (int c = 0; c < 2; ++c) {
+            uint32_t r[32];
+            if (ok) {
+                tmem_ld32(tmem + lane_base + kOCol + 64u * hf + 32u * c, r);
+                tmem_wait_ld();
+            }
+            float* const srow = slab + lane * kSlabStride + 32 * c;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                float4 v = make_float4(__uint_as_float(r[i]) * fn, __uint_as_float(r[i + 1]) * fn,
+                                       __uint_as_float(r[i + 2]) * fn, __uint_as_float(r[i + 3]) * fn);
+                if (!ok) v = make_float4(nan, nan, nan, nan);
                 if (p.merge) {
-                    const float4 u = od[c];
+                    const float4 u = *reinterpret_cast<const float4*>(srow + i);
                     v.x = fmaf(wo, u.x, v.x);
                     v.y = fmaf(wo, u.y, v.y);
                     v.z = fmaf(wo, u.z, v.z);
                     v.w = fmaf(wo, u.w, v.w);
                 }
-                od[c] = v;
+                *reinterpret_cast<float4*>(srow + i) = v;
             }
-            p.lse[gi] = lse;
         }
+        __syncwarp();
+#pragma unroll 4
+        for (int r2 = 0; r2 < 16; ++r2) {
+            const int rl = 2 * r2 + sub, tq = r0 + 32 * quarter + rl;
+            if (tq < q_len)
+                *reinterpret_cast<float4*>(p.o + ((int64_t)(q_begin + tq) * p.H + h) * kV + 64 * hf + 4 * c4) =
+                    *reinterpret_cast<const float4*>(slab + rl * kSlabStride + 4 * c4);
+        }
+        if (hf == 0 && live_row) p.lse[gi] = lse;
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) tmem_dealloc(tmem, 512);
+    if (warp == 8) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
@@ -502,9 +571,10 @@ cudaError_t launch_prefill_attn(const PrefillAttn& a, cudaStream_t s) {
             return e;
     }
     {
-        const uint64_t dims[3] = {128, (uint64_t)a.H, (uint64_t)a.key_rows};
-        const uint64_t strides[2] = {128 * 2, (uint64_t)a.H * 128 * 2};
-        const uint32_t box[3] = {64, 1, 128};
+        // head-major [H][key_rows][128]: one head's keys are contiguous 256-byte rows
+        const uint64_t dims[3] = {128, (uint64_t)a.key_rows, (uint64_t)a.H};
+        const uint64_t strides[2] = {128 * 2, (uint64_t)a.key_rows * 128 * 2};
+        const uint32_t box[3] = {64, 128, 1};
         if ((e = encode_tmap(&knm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.kn, dims, strides, box, true)) != cudaSuccess)
             return e;
         if ((e = encode_tmap(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v, dims, strides, box, true)) != cudaSuccess)
