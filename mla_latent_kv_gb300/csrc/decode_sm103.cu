@@ -55,7 +55,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (CTA 0) / 2-5 helpers (CTA 1)
+constexpr int kThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (CTA 0) / 2-5 helpers, 2-9 epilogue (CTA 1)
 constexpr int kPPG = 4;              // pages per group
 #ifndef MLA_PREFETCH_GROUPS
 #define MLA_PREFETCH_GROUPS 1
@@ -252,13 +252,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     int y[kPPG];
                     const int np = min(kPPG, npages - kPPG * gi);
                     for (int q = 0; q < np; ++q) y[q] = page_row<kFp8>(p, g.b, g.page0 + kPPG * gi + q);
-                    for (int q = 0; q < kPPG; ++q) {
-                        const int pg = kPPG * (gi + kPrefetchGroups) + q;
-                        if (pg >= npages) break;
-                        const int yr = page_row<kFp8>(p, g.b, g.page0 + pg);
-                        if (kFp8 || yr < p.num_blocks * kPage)
-                            bulk_prefetch_l2(kv_rows + (size_t)yr * kBf16RowBytes, kPage * kBf16RowBytes);
-                    }
+                    auto prefetch_ahead = [&]() {
+                        for (int q = 0; q < kPPG; ++q) {
+                            const int pg = kPPG * (gi + kPrefetchGroups) + q;
+                            if (pg >= npages) break;
+                            const int yr = page_row<kFp8>(p, g.b, g.page0 + pg);
+                            if (kFp8 || yr < p.num_blocks * kPage)
+                                bulk_prefetch_l2(kv_rows + (size_t)yr * kBf16RowBytes, kPage * kBf16RowBytes);
+                        }
+                    };
+                    // the first group's look-ahead waits until Q is on its way: every query
+                    // row's first MMA needs Q, and requests made earlier are served first
+                    if (gi > 0) prefetch_ahead();
                     for (int pn = 0; pn < 9; ++pn) {
                         const int m = 9 * gi + pn, slot = m % kSlots, k = m / kSlots;
                         if (!q_issued && m == 2) {  // Q: the preceding kernel's output
@@ -268,6 +273,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 tma_load_2d(sbase + q_panel_off(qn), &q_map, bar(B_QFULL), qn * 64, g.r * p.H);
                             tma_load_2d(sbase + OFF_QROPE, &q_map, bar(B_QFULL), 8 * 64, g.r * p.H);
                             q_issued = true;
+                            prefetch_ahead();
                         }
                         // first use of slots 2 and 3: Q's panels have been moved out to TMEM
                         ok = k > 0      ? wait_bar(bar(B_SLOTEMPTY + slot), (k - 1) & 1, abort, ds)
@@ -576,13 +582,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     wait_bar(bar(B_VEMPTY + i % kVStages), (i / kVStages) & 1, &dummy, nullptr);
                 }
             }
-        } else if (warp < 6) {
-            // ------------- helper warps: P / V arrival, rescale, tail zeroing, epilogue -------------
+        } else {
+            // ------------- helper warps 2-5: P / V arrival, rescale, tail zeroing -------------
+            // ------------- warps 2-9: the epilogue (each warp set stages half of the panels) ----
             const int row = 32 * (warp & 3) + lane;
             const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-            const int ctid = tid - 64;  // 0..127
-            int pages_ready = 0;
-            for (int i = 0; i < npages; ++i) {
+            const int ctid = tid - 64;  // 0..255; 0..127 are the helper warps
+            const int eset = warp >= 6 ? 1 : 0;
+            int pages_ready = warp >= 6 ? npages : 0;
+            for (int i = 0; i < npages && warp < 6; ++i) {
                 const int st = i % kVStages, kv = i / kVStages, pb = i % kPBufs, up = i / kPBufs;
                 if (!warp_wait(bar(B_PFULL + pb), up & 1, abort, ds)) break;
                 if (ctid == 0) {
@@ -638,7 +646,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const float inv = empty ? 0.f : 1.f / l;
             const float lse_v = empty ? -CUDART_INF_F : (m + log2f(lt)) * 0.6931471805599453f;
             const bool live = row < p.H;
-            if (live) {
+            if (live && eset == 0) {
                 const float lse_out = lse_v;
                 if (g.slot >= 0)
                     p.part_lse[(size_t)g.slot * p.H + row] = lse_out;
@@ -656,31 +664,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int rd = 0; rd < rounds; ++rd) {
                 if (rd > 0) {  // the previous round's stores have read their tiles
                     if (ctid == 0) bulk_wait_group_read<0>();
-                    named_bar(kBarEpi, 128);
+                    named_bar(kBarEpi, 256);
                 }
-#pragma unroll 1
-                for (int pl = 0; pl < 8; ++pl) {
-                    uint8_t* tile = smem + OFF_V + pl * kEpiPanelBytes;
-                    if (out_f32) {
-                        const int col0 = rd * 256 + pl * 32;
-                        uint32_t v[32];
-                        if (use_o) {
-                            tmem_ld32(tmem + lane_base + (uint32_t)col0, v);
-                            tmem_wait_ld();
-                        } else {
+                if (out_f32) {
+                    // this warp set's four 32-column panels: all TMEM loads, one wait, the stores
+                    uint32_t v[4][32];
+                    if (use_o) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = 0u;
-                        }
-                        if (live) {
+                        for (int q = 0; q < 4; ++q)
+                            tmem_ld32(tmem + lane_base + (uint32_t)(rd * 256 + (4 * eset + q) * 32), v[q]);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[q][j] = 0u;
+                    }
+                    if (live) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint8_t* tile = smem + OFF_V + (4 * eset + q) * kEpiPanelBytes;
 #pragma unroll
                             for (int c = 0; c < 8; ++c)
                                 *reinterpret_cast<uint4*>(tile + row * 128 + ((c ^ (row & 7)) << 4)) = make_uint4(
-                                    __float_as_uint(__uint_as_float(v[4 * c]) * inv),
-                                    __float_as_uint(__uint_as_float(v[4 * c + 1]) * inv),
-                                    __float_as_uint(__uint_as_float(v[4 * c + 2]) * inv),
-                                    __float_as_uint(__uint_as_float(v[4 * c + 3]) * inv));
+                                    __float_as_uint(__uint_as_float(v[q][4 * c]) * inv),
+                                    __float_as_uint(__uint_as_float(v[q][4 * c + 1]) * inv),
+                                    __float_as_uint(__uint_as_float(v[q][4 * c + 2]) * inv),
+                                    __float_as_uint(__uint_as_float(v[q][4 * c + 3]) * inv));
                         }
-                    } else {
+                    }
+                } else {
+                    // bf16: this warp set's four 64-column panels, one at a time
+#pragma unroll 1
+                    for (int pl = 4 * eset; pl < 4 * eset + 4; ++pl) {
+                        uint8_t* tile = smem + OFF_V + pl * kEpiPanelBytes;
                         const int col0 = pl * 64;
                         uint32_t v[2][32];
 #pragma unroll
@@ -707,7 +724,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 fence_proxy_async_cta();
-                named_bar(kBarEpi, 128);
+                named_bar(kBarEpi, 256);
                 if (ctid == 0) {
                     const int cpp = out_f32 ? 32 : 64;  // columns per panel
                     for (int pl = 0; pl < 8; ++pl)

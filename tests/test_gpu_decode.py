@@ -53,9 +53,10 @@ def test_causal_two_row_queries_and_empty_rows(num_splits):
     compare_decode(o, lse, o_ref, lse_ref)
 
 
-def test_bf16_output():
+@pytest.mark.parametrize("num_splits", [1, 2])  # 1: every row writes bf16 directly from the epilogue
+def test_bf16_output(num_splits):
     c = mi.decode_case(3, 1, 64, [5, 64, 300], seed=23)
-    o, lse, st = run_decode(c, 2, o_dtype=1)
+    o, lse, st = run_decode(c, num_splits, o_dtype=1)
     o_ref, lse_ref = _oracle(c)
     # one bf16 rounding of the output adds up to half an ulp of |o|
     compare_decode(o, lse, o_ref, lse_ref, extra_abs=float(np.abs(o_ref).max()) * 2.0 ** -9)
