@@ -122,3 +122,48 @@ def test_prefill_bad_block_id_is_reported():
     c["block_table"][0, 1] = c["num_blocks"] + 7
     o, lse, st = run_prefill(c, 64)
     assert st & 0x1
+
+
+def test_prefill_single_head():
+    c = mi.prefill_case([200, 3], [70, 2], H=1, seed=27)
+    o, lse, st = run_prefill(c, 128)
+    assert st == 0
+    compare(o, lse, *ref_prefill(c, 128))
+
+
+def test_prefill_fp8_many_chunks_and_query_tiles():
+    c = mi.prefill_case([700, 130, 0], [150, 5, 129], H=4, kv=mi.KV_FP8, seed=28)
+    rows = c["cache"].reshape(c["num_blocks"], 64, 584)
+    vs = rows[:, :, 580:584].copy().view("<f4") * np.float32(0.5)  # v_scale = k_scale / 2
+    rows[:, :, 580:584] = vs.view(np.uint8)
+    o, lse, st = run_prefill(c, 192)
+    assert st == 0
+    compare(o, lse, *ref_prefill(c, 192), fp8=True)
+
+
+def test_prefill_causal_only_three_query_tiles():
+    c = mi.prefill_case([0], [300], H=2, seed=29)
+    o, lse, st = run_prefill(c, 64)
+    assert st == 0
+    compare(o, lse, *ref_prefill(c, 64))
+
+
+def test_prefill_many_requests_packed_chunks():
+    rng = np.random.default_rng(30)
+    ctx = rng.integers(0, 400, size=20)
+    ctx[[2, 7]] = 0
+    ql = rng.integers(0, 40, size=20)
+    ql[[0, 5]] = [1, 130]
+    c = mi.prefill_case(list(ctx), list(ql), H=3, seed=30)
+    o, lse, st = run_prefill(c, 200)  # chunks hold several requests' rows
+    assert st == 0
+    compare(o, lse, *ref_prefill(c, 200))
+
+
+@pytest.mark.parametrize("chunk_rows", [64, 4096])
+def test_prefill_chunk_sizes_meet_the_same_bound(chunk_rows):
+    # a different chunking moves keys between tiles (other rounding of P); both meet the bound
+    c = mi.prefill_case([900, 450], [40, 100], H=2, seed=31)
+    o, lse, st = run_prefill(c, chunk_rows)
+    assert st == 0
+    compare(o, lse, *ref_prefill(c, chunk_rows))
