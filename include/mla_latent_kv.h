@@ -242,12 +242,14 @@ mla_status mla_cache_write(const void* kv_c, int64_t kv_c_stride_t, const void* 
  * Keys and values are up-projected per head, not absorbed:
  *     k_j = [ c_j . W_UK_T[h]^T (128) || k_pe_j (64) ],   v_j = c_j . W_UV[h]  (128)
  *     o[t, h, :] = sum_j softmax_j(scale * <q[t, h, :], k_j>) v_j,   lse[t, h] = ln sum_j exp(...)
- * over the request's context and its new tokens 0 .. t (causal). Run as the page describes:
- * the new tokens first (from kv_c / k_pe, not from the cache), then the context in chunks of at
- * most chunk_rows gathered rows (each request's context cut at page boundaries; the plan of
+ * over the request's context and its new tokens 0 .. t (causal); the new tokens' rows come from
+ * kv_c / k_pe, not from the cache. When the whole context fits in chunk_rows rows, one pass covers
+ * every request's context followed by its new tokens (the online softmax merges them). Otherwise
+ * the page's order runs: the new tokens first, then the context in chunks of at most chunk_rows
+ * gathered rows (each request's context cut at page boundaries; the plan of
  * mla_prefill_chunk_plan), every chunk's partial result merged into the running one by LSE
- * (merge_attn_states). FP8 rows are dequantised with k_scale on the key side (k_nope and k_pe)
- * and v_scale on the value side.
+ * (merge_attn_states). Both give the same attention. FP8 rows are dequantised with k_scale on the
+ * key side (k_nope and k_pe) and v_scale on the value side.
  *   q             bf16 [total_q, H, 192] contiguous: q_nope (128) || q_pe (64), RoPE applied
  *   kv_c, k_pe    bf16 new-token rows, element (t, d) at kv_c[t * kv_c_stride_t + d] (d < 512),
  *                 k_pe[t * k_pe_stride_t + r] (r < 64); strides multiples of 8
@@ -257,9 +259,11 @@ mla_status mla_cache_write(const void* kv_c, int64_t kv_c_stride_t, const void* 
  *                 memory (they size the launches and the chunk plan; no device read-back)
  *   W_UK_T        bf16 [H, 128, 512], W_UV bf16 [H, 512, 128] (the layouts of mla_absorb_q and
  *                 mla_out_proj)
- *   chunk_rows    context rows gathered and up-projected at a time, >= 64
- *   workspace     >= mla_prefill_workspace_bytes(B, total_q, H, chunk_rows) bytes, 256-byte
- *                 aligned, owned by the caller, contents undefined after the call
+ *   chunk_rows    context rows gathered and up-projected at a time, >= 64 (the page's budget is
+ *                 min(max(8 * max_len, 4 * max_seqs * 64), 65536) rows)
+ *   workspace     >= mla_prefill_workspace_bytes(B, total_q, H, chunk_rows) bytes (up-projected
+ *                 K / V for chunk_rows + total_q rows), 256-byte aligned, owned by the caller,
+ *                 contents undefined after the call
  *   o             fp32 [total_q, H, 128]; lse fp32 [total_q, H] or NULL
  * 1 <= H <= 128; 0 <= ctx_lens[b] <= max_blocks * 64. Bad block ids set MLA_DEV_BAD_BLOCK_ID,
  * a device ctx_lens value outside that range MLA_DEV_SEQ_TOO_LONG. Pointers 16-byte aligned.

@@ -273,7 +273,7 @@ def prefill_chunk_plan(ctx_lens, chunk_rows):
 
 
 def prefill(q, kv_c, k_pe, kv_cache, block_table, ctx_lens, query_start_loc, w_uk_t, w_uv, scale,
-            kv_dtype=KV_BF16, chunk_rows=8192, workspace=None, o=None, lse=None, dev_status=None, stream=None,
+            kv_dtype=KV_BF16, chunk_rows=None, workspace=None, o=None, lse=None, dev_status=None, stream=None,
             num_blocks=None, ctx_lens_host=None, query_start_loc_host=None):
     """Prefill through the compute-friendly route. q [total_q, H, 192] bf16 (q_nope || q_pe),
     kv_c [total_q, 512] / k_pe [total_q, 64] bf16 (the new tokens' rows, row-strided allowed),
@@ -289,6 +289,8 @@ def prefill(q, kv_c, k_pe, kv_cache, block_table, ctx_lens, query_start_loc, w_u
         else query_start_loc_host
     if num_blocks is None:
         num_blocks = kv_cache.numel() * kv_cache.element_size() // (PAGE * row_bytes(kv_dtype))
+    if chunk_rows is None:  # the page's 64k-row budget, no larger than this batch's context needs
+        chunk_rows = min(65536, max(PAGE, int(ctx_host.sum())))
     need = prefill_workspace_bytes(B, total_q, H, chunk_rows)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)

@@ -151,12 +151,16 @@ cudaError_t launch_up_proj_sm103(const uint16_t* x, int64_t x_st, int rows, cons
                                  uint16_t* out, int H, cudaStream_t s);
 
 // ---- prefill, the compute-friendly route ---------------------------------------------------
-// Rows of one segment (the new tokens, or one context chunk) gathered into a contiguous
-// workspace: the latent part x [rows, 512] and the rope part kpe [rows, 64], both bf16 holding
-// the stored values exactly (FP8 codes are not scaled here), plus per-row (k_scale, v_scale)
-// for an FP8 cache.
+// Rows of one segment gathered into a contiguous workspace: the latent part x [rows, 512] and the
+// rope part kpe [rows, 64], both bf16 holding the stored values exactly (FP8 codes are not scaled
+// here), plus per-row (k_scale, v_scale) for an FP8 cache (1 for rows taken from kv_c / k_pe).
+// Segments: the new tokens (kPrefillNew), one context chunk (kPrefillChunk), or every request's
+// context followed by its new tokens (kPrefillAll: request b's rows start at cu_ctx[b] + qsl[b]).
+enum { kPrefillChunk = 0, kPrefillNew = 1, kPrefillAll = 2 };
 struct PrefillGather {
-    const uint16_t* kv_c;       // new tokens: rows come from kv_c / k_pe (row strides st_c, st_pe)
+    int mode;
+    const int32_t* qsl;         // [B + 1] (kPrefillAll)
+    const uint16_t* kv_c;       // new tokens' rows (row strides st_c, st_pe)
     int64_t st_c;
     const uint16_t* k_pe;
     int64_t st_pe;
@@ -176,9 +180,10 @@ struct PrefillGather {
 };
 
 // One attention segment: every query row of the requests attends to its keys in the segment.
-// causal: the keys are the request's own new tokens (key i visible to query row t iff i <= t);
-// otherwise the keys are the request's rows of the context chunk [c0, c1) (all visible). The
-// result is written (merge = 0) or merged by LSE into o / lse (merge = 1).
+// kPrefillNew: the keys are the request's own new tokens (key i visible to query row t iff
+// i <= t). kPrefillChunk: the request's rows of the context chunk [c0, c1), all visible.
+// kPrefillAll: the request's context and then its new tokens (key p visible to query row t iff
+// p <= ctx + t). The result is written (merge = 0) or merged by LSE into o / lse (merge = 1).
 struct PrefillAttn {
     const uint16_t* q;          // [T, H, 192]
     const uint16_t* kn;         // [H, key_rows, 128] up-projected k_nope (head-major)
@@ -189,7 +194,7 @@ struct PrefillAttn {
     const int32_t* qsl;         // [B + 1]
     const int32_t* cu_ctx;      // [B + 1]
     int B, H, T, max_q_len;
-    int causal;
+    int mode;
     int64_t c0, c1;
     float scale;
     int merge;

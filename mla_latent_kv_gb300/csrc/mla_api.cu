@@ -385,7 +385,7 @@ struct PrefillLayout {
 PrefillLayout prefill_layout(int B, int total_q, int H, int64_t chunk_rows) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     PrefillLayout w{};
-    w.rows = std::max<int64_t>(total_q, chunk_rows);
+    w.rows = chunk_rows + total_q;  // one pass over context + new rows when the context fits
     size_t off = 0;
     w.cu_ctx = off;
     off += up((size_t)(B + 1) * sizeof(int32_t));
@@ -547,9 +547,39 @@ mla_status mla_prefill(const void* q, const void* kv_c, int64_t kv_c_stride_t, c
         if (err != cudaSuccess) return cuda_fail(err, "mla_prefill attention launch");
         return MLA_OK;
     };
+    // The whole context fits the row budget: one pass over every request's context followed by
+    // its new tokens, the same attention as the page's new-token segment, context chunks and
+    // merge, with the merge done by the online softmax itself.
+    if (total_ctx <= chunk_rows) {
+        mla::PrefillGather g{};
+        g.mode = mla::kPrefillAll;
+        g.qsl = query_start_loc;
+        g.kv_c = static_cast<const uint16_t*>(kv_c);
+        g.st_c = kv_c_stride_t;
+        g.k_pe = static_cast<const uint16_t*>(k_pe);
+        g.st_pe = k_pe_stride_t;
+        g.cache = static_cast<const uint8_t*>(kv_cache);
+        g.kv_dtype = kv_dtype;
+        g.num_blocks = num_blocks;
+        g.block_table = block_table;
+        g.max_blocks = max_blocks;
+        g.cu_ctx = cu_ctx;
+        g.B = B;
+        g.rows = (int)(total_ctx + total_q);
+        g.x = x;
+        g.kpe = kpe;
+        g.scales = scales;
+        g.dev_status = dev_status;
+        a.mode = mla::kPrefillAll;
+        a.merge = 0;
+        const mla_status st = segment(g, kv_dtype == MLA_KV_FP8_E4M3_SCALED);
+        if (st != MLA_OK) return st;
+        return ok();
+    }
     // 1. the new tokens, causal among themselves
     {
         mla::PrefillGather g{};
+        g.mode = mla::kPrefillNew;
         g.kv_c = static_cast<const uint16_t*>(kv_c);
         g.st_c = kv_c_stride_t;
         g.k_pe = static_cast<const uint16_t*>(k_pe);
@@ -557,7 +587,7 @@ mla_status mla_prefill(const void* q, const void* kv_c, int64_t kv_c_stride_t, c
         g.rows = total_q;
         g.x = x;
         g.kpe = kpe;
-        a.causal = 1;
+        a.mode = mla::kPrefillNew;
         a.merge = 0;
         const mla_status st = segment(g, false);
         if (st != MLA_OK) return st;
@@ -570,6 +600,7 @@ mla_status mla_prefill(const void* q, const void* kv_c, int64_t kv_c_stride_t, c
     auto flush = [&]() {
         if (cur < 0 || st != MLA_OK) return;
         mla::PrefillGather g{};
+        g.mode = mla::kPrefillChunk;
         g.cache = static_cast<const uint8_t*>(kv_cache);
         g.kv_dtype = kv_dtype;
         g.num_blocks = num_blocks;
@@ -583,7 +614,7 @@ mla_status mla_prefill(const void* q, const void* kv_c, int64_t kv_c_stride_t, c
         g.kpe = kpe;
         g.scales = scales;
         g.dev_status = dev_status;
-        a.causal = 0;
+        a.mode = mla::kPrefillChunk;
         a.merge = 1;
         a.c0 = c0;
         a.c1 = c1;

@@ -92,26 +92,37 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(PrefillGather
     if (i >= g.rows) return;
     uint4* const xd = reinterpret_cast<uint4*>(g.x + (int64_t)i * kL);
     uint4* const pd = reinterpret_cast<uint4*>(g.kpe + (int64_t)i * kR);
-    if (g.kv_c != nullptr) {  // the new tokens' own rows
-        const uint4* xs = reinterpret_cast<const uint4*>(g.kv_c + (int64_t)i * g.st_c);
-        const uint4* ps = reinterpret_cast<const uint4*>(g.k_pe + (int64_t)i * g.st_pe);
+    // workspace row -> a new token's row of kv_c / k_pe, or (request, position) in the cache
+    int64_t new_row = -1, pos = 0;
+    int lo = 0;
+    if (g.mode == kPrefillNew) {
+        new_row = i;
+    } else {
+        // the last request whose first row is <= this row
+        const int64_t gr = g.mode == kPrefillAll ? (int64_t)i : g.c0 + i;
+        int hi = g.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            const int64_t first = (int64_t)g.cu_ctx[mid] + (g.mode == kPrefillAll ? g.qsl[mid] : 0);
+            if (first <= gr)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        pos = gr - g.cu_ctx[lo] - (g.mode == kPrefillAll ? g.qsl[lo] : 0);
+        const int64_t ctx = g.cu_ctx[lo + 1] - g.cu_ctx[lo];
+        if (g.mode == kPrefillAll && pos >= ctx) new_row = g.qsl[lo] + (pos - ctx);
+    }
+    if (new_row >= 0) {  // a new token's own row, unscaled
+        const uint4* xs = reinterpret_cast<const uint4*>(g.kv_c + new_row * g.st_c);
+        const uint4* ps = reinterpret_cast<const uint4*>(g.k_pe + new_row * g.st_pe);
         const uint4 a = xs[lane], b = xs[lane + 32];
         xd[lane] = a;
         xd[lane + 32] = b;
         if (lane < 8) pd[lane] = ps[lane];
+        if (lane == 0 && g.scales) g.scales[i] = make_float2(1.f, 1.f);
         return;
     }
-    // packed context row -> (request, position): the last request whose first row is <= it
-    const int64_t gr = g.c0 + i;
-    int lo = 0, hi = g.B - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (g.cu_ctx[mid] <= gr)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    const int64_t pos = gr - g.cu_ctx[lo];
     const int64_t blk = g.block_table[(int64_t)lo * g.max_blocks + pos / kPage];
     if (blk < 0 || blk >= g.num_blocks) {
         if (lane == 0 && g.dev_status) atomicOr(g.dev_status, MLA_DEV_BAD_BLOCK_ID);
@@ -206,9 +217,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (r0 >= q_len) return;
     int64_t key0;  // first key row in the segment's workspace
     int n_keys;
-    if (p.causal) {
+    int shift = 0;  // causal segments: query row t sees keys [0, shift + t]
+    if (p.mode == kPrefillNew) {
         key0 = q_begin;
         n_keys = min(q_len, r0 + 128);  // the tile's last row sees new tokens 0 .. r0 + 127
+    } else if (p.mode == kPrefillAll) {
+        shift = p.cu_ctx[b + 1] - p.cu_ctx[b];  // the request's context precedes its new tokens
+        key0 = (int64_t)p.cu_ctx[b] + q_begin;
+        n_keys = shift + min(q_len, r0 + 128);
     } else {
         const int64_t g0 = max(p.c0, (int64_t)p.cu_ctx[b]);
         const int64_t g1 = min(p.c1, (int64_t)p.cu_ctx[b + 1]);
@@ -358,7 +374,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
         const uint32_t pair_bar = kBarPair0 + (uint32_t)quarter;
         const float sl2 = p.scale * 1.4426950408889634f;
-        const int limit = p.causal ? min(n_keys, t + 1) : n_keys;  // keys [0, limit) are visible
+        const int limit = p.mode != kPrefillChunk ? min(n_keys, shift + t + 1) : n_keys;  // keys [0, limit) visible
         float2* const sc = reinterpret_cast<float2*>(sgen + OFF_SC);
         float* const mx = reinterpret_cast<float*>(sgen + OFF_MX);  // [tile parity][hf][row]
         // running max m (exp2 domain) and the sum of this half's P relative to it
