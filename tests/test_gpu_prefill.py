@@ -167,3 +167,15 @@ def test_prefill_chunk_sizes_meet_the_same_bound(chunk_rows):
     o, lse, st = run_prefill(c, chunk_rows)
     assert st == 0
     compare(o, lse, *ref_prefill(c, chunk_rows))
+
+
+def test_prefill_fp8_one_pass():
+    # the whole context fits the row budget: context rows (e4m3 widened, per-row scales) and the
+    # new tokens' rows (scale 1) share one workspace and one attention pass
+    c = mi.prefill_case([90, 0, 200, 333], [4, 6, 150, 9], H=3, kv=mi.KV_FP8, seed=32)
+    rows = c["cache"].reshape(c["num_blocks"], 64, 584)
+    vs = rows[:, :, 580:584].copy().view("<f4") * np.float32(2.0)  # v_scale = 2 k_scale
+    rows[:, :, 580:584] = vs.view(np.uint8)
+    o, lse, st = run_prefill(c, 4096)
+    assert st == 0
+    compare(o, lse, *ref_prefill(c, 4096), fp8=True)
