@@ -10,10 +10,10 @@
 //   2. the context, in chunks of at most chunk_rows gathered rows; each chunk's result is merged
 //      into the running one by LSE in the attention kernel's epilogue (merge_attn_states).
 //
-// Attention kernel: one CTA per (128-query tile, request, head), 320 threads, 1 CTA per SM.
-//   warp 8 lane 0   TMA: the q tile (three 64-dim panels); per 128-key tile the K panels (k_nope dims 0-63 and 64-127 of this head,
-//                   k_pe shared by all heads) into a 2-stage ring and, one tile behind, the two
-//                   V panels into another 2-stage ring
+// Attention kernel: one CTA per (128-query tile, request, head), 352 threads, 1 CTA per SM.
+//   warp 8 lane 0   TMA: the q tile (three 64-dim panels); per 128-key tile the K panels (k_nope
+//                   dims 0-63 and 64-127 of this head, k_pe shared by all heads) into a 2-stage ring
+//   warp 10 lane 0  TMA: per 128-key tile the two V panels into another 2-stage ring
 //   warp 9 lane 0   tcgen05.mma: S_j = Q K_j^T (M = 128 queries, N = 128 keys, K = 192, both
 //                   operands in shared memory) into one of three 128-column TMEM buffers, one key
 //                   tile ahead of O += P_{j-1} V_{j-1} (P read from TMEM over S, V an MN-major
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(PrefillGather
 }
 
 // ---------------------------------------------------------------- attention
-constexpr int kAttnThreads = 320;       // warps 0-7 softmax, 8 TMA + TMEM, 9 MMA
+constexpr int kAttnThreads = 352;       // warps 0-7 softmax, 8 TMA (q, K) + TMEM, 9 MMA, 10 TMA (V)
 constexpr int kPanel = 128 * 128;       // 128 rows x 64 bf16 (128-byte swizzle): 16 KB
 constexpr int OFF_Q = 0;                // 3 panels (the A operand of QK)
 constexpr int OFF_K = 3 * kPanel;       // 2 stages x 3 panels (k_nope 0-63, 64-127, k_pe)
@@ -268,34 +268,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     volatile int* abort = &abort_flag;
 
     if (warp == 8) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ TMA producer: q and K
         if (lane == 0) {
             tma_prefetch_desc(&q_map);
             tma_prefetch_desc(&kn_map);
             tma_prefetch_desc(&kpe_map);
-            tma_prefetch_desc(&v_map);
             bar_arrive_expect_tx(bar(B_Q), 3 * kPanel);
             for (int pn = 0; pn < 3; ++pn)
                 tma_load_3d(sbase + OFF_Q + pn * kPanel, &q_map, bar(B_Q), 64 * pn, h, q_begin + r0);
-            int klast[2] = {-1, -1}, vlast[2] = {-1, -1};
-            auto load_v = [&](int j) -> bool {
+            int klast[2] = {-1, -1};
+            for (int j = 0; j < n_tiles; ++j) {
                 const int st = j & 1;
-                if (j >= 2 && !wait_bar(bar(B_VEMPTY + st), ((j >> 1) - 1) & 1, abort, ds)) return false;
-                const uint32_t dst = sbase + OFF_V + st * 2 * kPanel;
-                const int z = (int)(key0 + 128 * j);
-                bar_arrive_expect_tx(bar(B_VFULL + st), 2 * kPanel);
-                tma_load_3d(dst, &v_map, bar(B_VFULL + st), 0, z, h);
-                tma_load_3d(dst + kPanel, &v_map, bar(B_VFULL + st), 64, z, h);
-                vlast[st] = j;
-                return true;
-            };
-            bool ok = true;
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !wait_bar(bar(B_KEMPTY + st), ((j >> 1) - 1) & 1, abort, ds)) {
-                    ok = false;
-                    break;
-                }
+                if (j >= 2 && !wait_bar(bar(B_KEMPTY + st), ((j >> 1) - 1) & 1, abort, ds)) break;
                 const uint32_t dst = sbase + OFF_K + st * 3 * kPanel;
                 const int z = (int)(key0 + 128 * j);
                 bar_arrive_expect_tx(bar(B_KFULL + st), 3 * kPanel);
@@ -303,15 +287,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 tma_load_3d(dst + kPanel, &kn_map, bar(B_KFULL + st), 64, z, h);
                 tma_load_2d(dst + 2 * kPanel, &kpe_map, bar(B_KFULL + st), 0, z);
                 klast[st] = j;
-                if (j >= 1) ok = load_v(j - 1);  // V one tile behind: it is needed after the softmax
             }
-            if (ok) load_v(n_tiles - 1);
             // every copy issued has landed before the CTA can leave
             int ignore = 0;
             wait_bar(bar(B_Q), 0, &ignore, nullptr);
             for (int st = 0; st < 2; ++st) {
                 ignore = 0;
                 if (klast[st] >= 0) wait_bar(bar(B_KFULL + st), (klast[st] >> 1) & 1, &ignore, nullptr);
+            }
+        }
+    } else if (warp == 10) {
+        // ------------------------------------------------------------ TMA producer: V
+        // A thread of its own, so that a V stage still in use never holds back the next K tile.
+        if (lane == 0) {
+            tma_prefetch_desc(&v_map);
+            int vlast[2] = {-1, -1};
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !wait_bar(bar(B_VEMPTY + st), ((j >> 1) - 1) & 1, abort, ds)) break;
+                const uint32_t dst = sbase + OFF_V + st * 2 * kPanel;
+                const int z = (int)(key0 + 128 * j);
+                bar_arrive_expect_tx(bar(B_VFULL + st), 2 * kPanel);
+                tma_load_3d(dst, &v_map, bar(B_VFULL + st), 0, z, h);
+                tma_load_3d(dst + kPanel, &v_map, bar(B_VFULL + st), 64, z, h);
+                vlast[st] = j;
+            }
+            int ignore = 0;
+            for (int st = 0; st < 2; ++st) {
                 ignore = 0;
                 if (vlast[st] >= 0) wait_bar(bar(B_VFULL + st), (vlast[st] >> 1) & 1, &ignore, nullptr);
             }
