@@ -65,14 +65,25 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+DECODE_SOURCES = ("decode_sm103.cu", "sm103_ptx.cuh", "internal.h")  # what the decode kernel compiles from
+
+
+def decode_kernel_sha256():
+    """sha256 over the decode kernel's source files, in DECODE_SOURCES order."""
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "mla_latent_kv_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def measured_traffic(workload):
     """DRAM bytes per decode launch from the committed ncu capture (profiles/traffic.json), or
     None when that capture was of another workload or of a different decode kernel source."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)["decode_sm103.cu"]
-        with open(os.path.join(ROOT, "mla_latent_kv_gb300", "csrc", "decode_sm103.cu"), "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()
+        h = decode_kernel_sha256()
     except (OSError, KeyError, ValueError):
         return None
     if rec.get("sha256") != h or rec.get("workload") != workload:

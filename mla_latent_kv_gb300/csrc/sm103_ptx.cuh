@@ -109,10 +109,11 @@ __device__ __forceinline__ bool bar_try_wait_cluster(uint32_t bar, uint32_t pari
     return ok != 0;
 }
 
-// Bounded wait for the completion of the phase with the given parity. Returns false (after
-// setting *abort and the device status bit) if the CTA is aborting or the wait timed out.
-template <bool kClusterScope = false>
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* dev_status) {
+// The polling loop of wait_bar(), kept out of line: inlined at every wait, the loop costs a
+// waiting thread about 100 cycles even when the phase has already completed, which a thread that
+// issues MMAs between waits pays in tensor-pipe time.
+template <bool kClusterScope>
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* dev_status) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
         bool done = kClusterScope ? bar_try_wait_cluster(bar, parity) : bar_try_wait(bar, parity);
@@ -129,6 +130,16 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
             }
         }
     }
+}
+
+// Bounded wait for the completion of the phase with the given parity. Returns false (after
+// setting *abort and the device status bit) if the CTA is aborting or the wait timed out.
+// One probe inline (the common case: the phase has completed), the polling loop out of line.
+template <bool kClusterScope = false>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* dev_status) {
+    const bool done = kClusterScope ? bar_try_wait_cluster(bar, parity) : bar_try_wait(bar, parity);
+    if (__builtin_expect(done, 1)) return true;
+    return wait_bar_slow<kClusterScope>(bar, parity, abort, dev_status);
 }
 
 // ------------------------------------------------------------------------------------------
