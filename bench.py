@@ -52,6 +52,9 @@ def parse():
                     help="-1: GB300 planner, 0: the pages' Triton rule, >0 forced")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--o-dtype", default="bf16", choices=["bf16", "fp32"],
+                    help="dtype of o_latent and o: the model dtype (bf16) that the attention output is kept "
+                         "in, or fp32; the LSE and split-KV partials are fp32 either way")
     ap.add_argument("--flush-mb", type=int, default=256, help="L2 flush buffer written between steps")
     return ap.parse_args()
 
@@ -79,16 +82,18 @@ def decode_kernel_sha256():
 
 def measured_traffic(workload):
     """DRAM bytes per decode launch from the committed ncu capture (profiles/traffic.json), or
-    None when that capture was of another workload or of a different decode kernel source."""
+    None when that capture was of another workload (name and o_latent dtype, e.g. "dsv3/o_bf16")
+    or of a different decode kernel source."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)["decode_sm103.cu"]
         h = decode_kernel_sha256()
     except (OSError, KeyError, ValueError):
         return None
-    if rec.get("sha256") != h or rec.get("workload") != workload:
+    w = rec.get("workloads", {}).get(workload)
+    if rec.get("sha256") != h or w is None:
         return None
-    return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
+    return int(w["dram_bytes_read"]) + int(w["dram_bytes_write"])
 
 
 def workload_inputs(name, seed_offset=0):
@@ -103,17 +108,17 @@ def workload_inputs(name, seed_offset=0):
     return c
 
 
-def algorithmic(c):
+def algorithmic(c, o_bytes=4):
     """Bytes and flops one decode launch must move / do (the absorbed algorithm, nothing else):
-    KV rows of every visible token + q + o_latent (fp32) + lse + block-table entries + seq_lens;
-    flops 2 * (576 + 512) per (query row, visible token, head)."""
+    KV rows of every visible token + q + o_latent (o_bytes per element) + lse + block-table entries
+    + seq_lens; flops 2 * (576 + 512) per (query row, visible token, head)."""
     B, Sq, H = c["B"], c["Sq"], c["H"]
     rb = mi.ROW_BYTES[c["kv"]]
     lens = np.asarray(c["seq_lens"], np.int64)
     n_rows = np.array([[max(0, int(s) - (Sq - 1 - t)) for t in range(Sq)] for s in lens])
     kv_bytes = int(lens.sum()) * rb  # each request's rows are read once for all its query rows
     pages = int(((lens + 63) // 64).sum())
-    byts = kv_bytes + B * Sq * H * (576 * 2 + 512 * 4 + 4) + pages * 4 + B * 4
+    byts = kv_bytes + B * Sq * H * (576 * 2 + 512 * o_bytes + 4) + pages * 4 + B * 4
     flops = int(n_rows.sum()) * H * 2 * (576 + 512)
     return byts, flops, kv_bytes
 
@@ -273,9 +278,10 @@ def run_ours(args):
     ws_n = mla.workspace_bytes(B, Sq, H, S, c["kv"], max_len)
     ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
     q = torch.empty((T, H, mi.D), dtype=torch.bfloat16, device=dev)
-    o_lat = torch.empty((B, Sq, H, mi.L), dtype=torch.float32, device=dev)
+    odt = torch.bfloat16 if args.o_dtype == "bf16" else torch.float32
+    o_lat = torch.empty((B, Sq, H, mi.L), dtype=odt, device=dev)
     lse = torch.empty((B, Sq, H), dtype=torch.float32, device=dev)
-    o = torch.empty((T, H, mi.V), dtype=torch.float32, device=dev)
+    o = torch.empty((T, H, mi.V), dtype=odt, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(args.flush_mb * (1 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -342,7 +348,7 @@ def run_ours(args):
     sets = [dict(qn=torch.empty_like(q_nope), qp=torch.empty_like(q_pe), bt=torch.empty_like(bt),
                  sl=torch.empty_like(sl), q=torch.empty_like(q), ol=torch.empty_like(o_lat), lse=torch.empty_like(lse),
                  o=torch.empty_like(o), ws=torch.empty_like(ws),
-                 h_o=torch.empty((T, H, mi.V), dtype=torch.float32).pin_memory()) for _ in range(2)]
+                 h_o=torch.empty((T, H, mi.V), dtype=odt).pin_memory()) for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     sync_ev = lambda: torch.cuda.Event()  # noqa: E731
 
@@ -400,7 +406,8 @@ def run_ours(args):
         return
 
     peaks, peak_src = load_peaks()
-    byts, flops, kv_bytes = algorithmic(c)
+    byts, flops, kv_bytes = algorithmic(c, o_bytes=2 if args.o_dtype == "bf16" else 4)
+    traffic_key = f"{args.workload}/o_{args.o_dtype}"
     dec_s = dec_ms * 1e-3
     gbs = byts / dec_s / 1e9
     tflops = flops / dec_s / 1e12
@@ -409,11 +416,11 @@ def run_ours(args):
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs / peaks["hbm_gbs"], "traffic": measured_traffic(args.workload)}
+                "frac": gbs / peaks["hbm_gbs"], "traffic": measured_traffic(traffic_key)}
     else:
         pk = peaks["bf16_tflops_sustained"]
         roof = {"bound": "tensor", "achieved": tflops, "peak": pk, "unit": "TFLOP/s", "frac": tflops / pk,
-                "traffic": measured_traffic(args.workload)}
+                "traffic": measured_traffic(traffic_key)}
     roof.update({"kernel": "mla_decode", "peak_source": f"{peak_src} (MEASURED_PEAKS.json)",
                  "bytes_per_launch": byts, "flops_per_launch": flops,
                  "min_roofline_frac": max(t_hbm, t_tc) / dec_s})
@@ -434,6 +441,7 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": workload_name(args.workload), "B": B, "Sq": Sq, "H": H,
                        "kv_dtype": "fp8" if c["kv"] == mi.KV_FP8 else "bf16", "num_splits": S,
+                       "o_dtype": args.o_dtype,
                        "l2": f"KV {kv_bytes / 1e6:.0f} MB > L2, plus a {args.flush_mb} MB L2 flush between steps",
                        "decode_timing": "CUDA events around mla_decode on every 8th timed step",
                        "e2e_timing": "pinned host inputs copied in and the result copied out every step, two "

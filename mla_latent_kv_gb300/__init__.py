@@ -150,8 +150,34 @@ def absorb_q(q_nope, q_pe, w_uk_t, out=None, stream=None):
     return out
 
 
+def _dt_code(buf, dt):
+    """The output dtype code: `dt` when given, else the given buffer's dtype, else fp32."""
+    import torch
+    if dt is not None:
+        return dt
+    if buf is not None and buf.dtype == torch.bfloat16:
+        return DT_BF16
+    return DT_F32
+
+
+def _out_buf(buf, shape, dt, device):
+    """An output buffer of dtype code `dt` holding `shape`: made when not given; a given one must be
+    contiguous, of that dtype and at least that large, since the kernels write through its pointer."""
+    import torch
+    tdt = torch.float32 if dt == DT_F32 else torch.bfloat16
+    if buf is None:
+        return torch.empty(shape, dtype=tdt, device=device)
+    n = 1
+    for d in shape:
+        n *= int(d)
+    if buf.dtype != tdt or buf.numel() < n or not buf.is_contiguous():
+        raise ValueError(f"output buffer must be a contiguous {tdt} of at least {n} elements, "
+                         f"got {buf.dtype} with {buf.numel()} (contiguous={buf.is_contiguous()})")
+    return buf
+
+
 def decode(q, kv_cache, block_table, seq_lens, max_seq_len, scale, kv_dtype=KV_BF16, num_splits=0,
-           workspace=None, o_latent=None, o_dtype=DT_F32, lse=None, dev_status=None, stream=None,
+           workspace=None, o_latent=None, o_dtype=None, lse=None, dev_status=None, stream=None,
            num_blocks=None):
     """q [B,Sq,H,576] bf16, kv_cache [num_blocks, 64*row_bytes] uint8 (or a bf16 view), block_table
     [B,max_blocks] int32, seq_lens [B] int32 -> (o_latent [B,Sq,H,512], lse [B,Sq,H])."""
@@ -164,11 +190,9 @@ def decode(q, kv_cache, block_table, seq_lens, max_seq_len, scale, kv_dtype=KV_B
     need = workspace_bytes(B, Sq, H, S, kv_dtype, max_seq_len)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-    if o_latent is None:
-        o_latent = torch.empty((B, Sq, H, L), dtype=torch.float32 if o_dtype == DT_F32 else torch.bfloat16,
-                               device=dev)
-    if lse is None:
-        lse = torch.empty((B, Sq, H), dtype=torch.float32, device=dev)
+    o_dtype = _dt_code(o_latent, o_dtype)
+    o_latent = _out_buf(o_latent, (B, Sq, H, L), o_dtype, dev)
+    lse = _out_buf(lse, (B, Sq, H), DT_F32, dev)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().mla_decode(_p(q), _p(kv_cache), kv_dtype, int(num_blocks), _p(block_table),
                             block_table.shape[1], _p(seq_lens), int(max_seq_len), B, Sq, H, float(scale),
@@ -182,7 +206,7 @@ def noalloc_max_workspace_bytes() -> int:
 
 
 def decode_noalloc(q, kv_cache, block_table, seq_lens, max_seq_len, scale, kv_dtype=KV_BF16, num_splits=0,
-                   o_latent=None, o_dtype=DT_F32, lse=None, dev_status=None, stream=None, num_blocks=None):
+                   o_latent=None, o_dtype=None, lse=None, dev_status=None, stream=None, num_blocks=None):
     """decode() through mla_decode_noalloc: the split-KV scratch is the library's own fixed device
     array, so no workspace is passed (outputs are still made here when not given)."""
     import torch
@@ -190,11 +214,9 @@ def decode_noalloc(q, kv_cache, block_table, seq_lens, max_seq_len, scale, kv_dt
     dev = q.device
     if num_blocks is None:
         num_blocks = kv_cache.numel() * kv_cache.element_size() // (PAGE * row_bytes(kv_dtype))
-    if o_latent is None:
-        o_latent = torch.empty((B, Sq, H, L), dtype=torch.float32 if o_dtype == DT_F32 else torch.bfloat16,
-                               device=dev)
-    if lse is None:
-        lse = torch.empty((B, Sq, H), dtype=torch.float32, device=dev)
+    o_dtype = _dt_code(o_latent, o_dtype)
+    o_latent = _out_buf(o_latent, (B, Sq, H, L), o_dtype, dev)
+    lse = _out_buf(lse, (B, Sq, H), DT_F32, dev)
     _check(lib().mla_decode_noalloc(_p(q), _p(kv_cache), kv_dtype, int(num_blocks), _p(block_table),
                                     block_table.shape[1], _p(seq_lens), int(max_seq_len), B, Sq, H, float(scale),
                                     int(num_splits), _p(o_latent), o_dtype, _p(lse), _p(dev_status),
@@ -203,7 +225,7 @@ def decode_noalloc(q, kv_cache, block_table, seq_lens, max_seq_len, scale, kv_dt
 
 
 def decode_varlen(q, kv_cache, block_table, seq_lens, query_start_loc, max_seq_len, scale, kv_dtype=KV_BF16,
-                  num_splits=0, workspace=None, o_latent=None, o_dtype=DT_F32, lse=None, dev_status=None, stream=None,
+                  num_splits=0, workspace=None, o_latent=None, o_dtype=None, lse=None, dev_status=None, stream=None,
                   num_blocks=None):
     """q [total_q, H, 576] bf16 packed by query_start_loc [B + 1] int32 (device) ->
     (o_latent [total_q, H, 512], lse [total_q, H])."""
@@ -217,11 +239,9 @@ def decode_varlen(q, kv_cache, block_table, seq_lens, query_start_loc, max_seq_l
     need = int(lib().mla_decode_varlen_workspace_bytes(kv_dtype, B, total_q, H, S, max_seq_len))
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-    if o_latent is None:
-        o_latent = torch.empty((total_q, H, L), dtype=torch.float32 if o_dtype == DT_F32 else torch.bfloat16,
-                               device=dev)
-    if lse is None:
-        lse = torch.empty((total_q, H), dtype=torch.float32, device=dev)
+    o_dtype = _dt_code(o_latent, o_dtype)
+    o_latent = _out_buf(o_latent, (total_q, H, L), o_dtype, dev)
+    lse = _out_buf(lse, (total_q, H), DT_F32, dev)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().mla_decode_varlen(_p(q), _p(kv_cache), kv_dtype, int(num_blocks), _p(block_table),
                                    block_table.shape[1], _p(seq_lens), _p(query_start_loc), int(max_seq_len), B,
@@ -243,14 +263,16 @@ def cache_write(kv_c, k_pe, slot_mapping, kv_cache, kv_dtype=KV_BF16, kv_scale=0
     return kv_cache
 
 
-def out_proj(o_latent, w_uv, out=None, out_dtype=DT_F32, stream=None):
-    """o_latent [T,H,512] fp32/bf16, W_UV [H,512,128] bf16 -> o [T,H,128]."""
+def out_proj(o_latent, w_uv, out=None, out_dtype=None, stream=None):
+    """o_latent [T,H,512] fp32/bf16, W_UV [H,512,128] bf16 -> o [T,H,128] (fp32 unless out_dtype or
+    a given `out` says bf16)."""
     import torch
     T, H = o_latent.shape[0], o_latent.shape[1]
+    if o_latent.dtype not in (torch.float32, torch.bfloat16) or not o_latent.is_contiguous():
+        raise ValueError(f"o_latent must be a contiguous fp32 or bf16 tensor, got {o_latent.dtype}")
     in_dtype = DT_F32 if o_latent.dtype == torch.float32 else DT_BF16
-    if out is None:
-        out = torch.empty((T, H, V), dtype=torch.float32 if out_dtype == DT_F32 else torch.bfloat16,
-                          device=o_latent.device)
+    out_dtype = _dt_code(out, out_dtype)
+    out = _out_buf(out, (T, H, V), out_dtype, o_latent.device)
     _check(lib().mla_out_proj(_p(o_latent), in_dtype, _p(w_uv), _p(out), out_dtype, T, H, _stream(stream)))
     return out
 

@@ -166,3 +166,25 @@ def test_prefill_rejects_bad_arguments_before_any_launch(lib):
     assert call(ws_bytes=100) == mla.ERR_WORKSPACE_TOO_SMALL
     # nothing to do: no query rows
     assert call(qsl_h=np.array([0, 0, 0], np.int32)) == mla.OK
+
+
+def test_binding_output_buffers_match_their_dtype_code():
+    # the kernels write through the output pointer with the element size of the dtype code, so
+    # the binding derives the code from a given buffer and refuses one that does not fit it
+    import torch
+    import mla_latent_kv_gb300 as mla
+    bf = torch.empty((2, 3, 512), dtype=torch.bfloat16)
+    f32 = torch.empty((2, 3, 512), dtype=torch.float32)
+    assert mla._dt_code(None, None) == mla.DT_F32
+    assert mla._dt_code(bf, None) == mla.DT_BF16
+    assert mla._dt_code(f32, None) == mla.DT_F32
+    assert mla._dt_code(bf, mla.DT_F32) == mla.DT_F32  # an explicit code wins, and is then checked
+    assert mla._out_buf(bf, (2, 3, 512), mla.DT_BF16, "cpu") is bf
+    made = mla._out_buf(None, (4, 5), mla.DT_BF16, "cpu")
+    assert made.dtype == torch.bfloat16 and tuple(made.shape) == (4, 5)
+    with pytest.raises(ValueError):
+        mla._out_buf(bf, (2, 3, 512), mla.DT_F32, "cpu")  # fp32 rows into a bf16 buffer
+    with pytest.raises(ValueError):
+        mla._out_buf(f32, (2, 4, 512), mla.DT_F32, "cpu")  # too small
+    with pytest.raises(ValueError):
+        mla._out_buf(f32.transpose(0, 1), (3, 2, 512), mla.DT_F32, "cpu")  # not contiguous
