@@ -81,6 +81,16 @@ const char* mla_status_string(mla_status s);
 /* Detail of the last failing call on this host thread ("" if none). Never NULL. */
 const char* mla_last_error_detail(void);
 
+/* Self-test of the bounded-wait path that guards every pipeline wait in the kernels: one thread
+ * waits on an mbarrier that nothing arrives on. The wait gives up after the library's limit (2 s
+ * of global time), ORs MLA_DEV_WAIT_TIMEOUT into *dev_status and the kernel returns.
+ *   dev_status  device int32, caller-owned (zero it first)
+ *   out         device int32[2], caller-owned: out[0] = milliseconds the wait took, out[1] = 1 if
+ *               the wait reported success (it must not), else 0
+ * Asynchronous on `stream`; read both after a synchronise. MLA_ERR_INVALID_ARG if a pointer is
+ * NULL, MLA_ERR_CUDA if the launch fails. */
+mla_status mla_selftest_wait_timeout(int32_t* dev_status, int32_t* out, mla_stream_t stream);
+
 /* Bytes of one cached token row: 1152 (bf16) or 584 (FP8), -1 for an unknown format
  * ([vLLM-MLA, cache shape section]; [vLLM-MLA, numbers section]). Host only. */
 int64_t mla_kv_row_bytes(mla_kv_dtype kv_dtype);

@@ -47,6 +47,8 @@ def lib() -> ctypes.CDLL:
         l.mla_status_string.argtypes = [i32]
         l.mla_last_error_detail.restype = ctypes.c_char_p
         l.mla_last_error_detail.argtypes = []
+        l.mla_selftest_wait_timeout.restype = i32
+        l.mla_selftest_wait_timeout.argtypes = [vp, vp, vp]
         l.mla_kv_row_bytes.restype = i64
         l.mla_kv_row_bytes.argtypes = [i32]
         l.mla_default_num_splits.restype = i32
@@ -199,6 +201,12 @@ def decode(q, kv_cache, block_table, seq_lens, max_seq_len, scale, kv_dtype=KV_B
                             int(S), _p(workspace), ws_bytes, _p(o_latent), o_dtype, _p(lse), _p(dev_status),
                             _stream(stream)))
     return o_latent, lse
+
+
+def selftest_wait_timeout(dev_status, out, stream=None):
+    """Run the bounded-wait self-test: dev_status int32 [1] and out int32 [2] on the device; after a
+    synchronise dev_status has MLA_DEV_WAIT_TIMEOUT set, out[0] is the wait in ms, out[1] is 0."""
+    _check(lib().mla_selftest_wait_timeout(_p(dev_status), _p(out), _stream(stream)))
 
 
 def noalloc_max_workspace_bytes() -> int:

@@ -188,3 +188,8 @@ def test_binding_output_buffers_match_their_dtype_code():
         mla._out_buf(f32, (2, 4, 512), mla.DT_F32, "cpu")  # too small
     with pytest.raises(ValueError):
         mla._out_buf(f32.transpose(0, 1), (3, 2, 512), mla.DT_F32, "cpu")  # not contiguous
+
+
+def test_selftest_rejects_null_pointers_before_any_launch(lib):
+    import mla_latent_kv_gb300 as mla
+    assert lib.mla_selftest_wait_timeout(None, None, None) == mla.ERR_INVALID_ARG
