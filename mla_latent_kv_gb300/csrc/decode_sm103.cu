@@ -22,8 +22,10 @@
 //                     the group for 32 heads; fp32 online softmax with a lazily moved running
 //                     max (rescale only when a row's max grows by more than 2^8). P (bf16, in
 //                     the MMA's swizzled K-major layout) and the per-head rescale factors are
-//                     written to local staging buffers and sent to CTA 1 with one bulk
-//                     shared-to-shared copy per page (counted by bytes on CTA 1's barrier).
+//                     written to four one-page staging buffers. A copier warp sends each staged
+//                     page to CTA 1 with one bulk shared-to-shared copy (counted by bytes on CTA
+//                     1's barrier) once CTA 1's buffer for it is free, so the softmax warps never
+//                     wait on CTA 1 and the next group's softmax overlaps CTA 1's PV.
 //   CTA 1 ("output")  holds the 128 x 512 fp32 output accumulator -- all 512 TMEM columns of its
 //                     SM, the reason the work is split over two SMs -- streams the pages'
 //                     first 512 dims (mostly L2 hits), and accumulates O += P V per page with
