@@ -10,14 +10,15 @@
 //   2. the context, in chunks of at most chunk_rows gathered rows; each chunk's result is merged
 //      into the running one by LSE in the attention kernel's epilogue (merge_attn_states).
 //
-// Attention kernel: one CTA per (128-query tile, request, head), 352 threads, 1 CTA per SM.
+// Attention kernel: one CTA per (128-query tile, request, head), 384 threads, 1 CTA per SM.
 //   warp 8 lane 0   TMA: the q tile (three 64-dim panels); per 128-key tile the K panels (k_nope
 //                   dims 0-63 and 64-127 of this head, k_pe shared by all heads) into a 2-stage ring
 //   warp 10 lane 0  TMA: per 128-key tile the two V panels into another 2-stage ring
 //   warp 9 lane 0   tcgen05.mma: S_j = Q K_j^T (M = 128 queries, N = 128 keys, K = 192, both
-//                   operands in shared memory) into one of three 128-column TMEM buffers, one key
-//                   tile ahead of O += P_{j-1} V_{j-1} (P read from TMEM over S, V an MN-major
-//                   operand in shared memory)
+//                   operands in shared memory) into one of three 128-column TMEM buffers
+//   warp 11 lane 0  tcgen05.mma: O += P_j V_j (P read from TMEM over S, V an MN-major operand in
+//                   shared memory); two issuing threads, so that one's waits leave the pipe busy
+//                   with the other's MMAs
 //   warps 0-7       softmax, two warps per TMEM lane quarter (one query row per lane, 64 key
 //                   columns per warp): fp32 online softmax in the exp2 domain with a lazily moved
 //                   running max (O and l are rescaled only when a row's max grows by more than
@@ -163,7 +164,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(PrefillGather
 }
 
 // ---------------------------------------------------------------- attention
-constexpr int kAttnThreads = 352;       // warps 0-7 softmax, 8 TMA (q, K) + TMEM, 9 MMA, 10 TMA (V)
+constexpr int kAttnThreads = 384;       // warps 0-7 softmax, 8 TMA (q, K) + TMEM, 9 QK MMAs, 10 TMA (V), 11 PV MMAs
 constexpr int kPanel = 128 * 128;       // 128 rows x 64 bf16 (128-byte swizzle): 16 KB
 constexpr int OFF_Q = 0;                // 3 panels (the A operand of QK)
 constexpr int OFF_K = 3 * kPanel;       // 2 stages x 3 panels (k_nope 0-63, 64-127, k_pe)
@@ -187,8 +188,9 @@ enum {
     B_SFULL = 9,    // 3
     B_PREADY = 12,  // 3 (256 arrivals)
     B_PVDONE = 15,  // 3
-    B_FINAL = 18,
-    kNumBars = 19
+    B_FINAL = 18,     // the PV thread's MMAs have completed
+    B_FINAL_QK = 19,  // the QK thread's MMAs have completed
+    kNumBars = 20
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* ds) {
@@ -255,6 +257,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             bar_init(bar(B_PVDONE + i), 1);
         }
         bar_init(bar(B_FINAL), 1);
+        bar_init(bar(B_FINAL_QK), 1);
         fence_barrier_init();
     }
     if (warp == 8) {
@@ -318,51 +321,57 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (vlast[st] >= 0) wait_bar(bar(B_VFULL + st), (vlast[st] >> 1) & 1, &ignore, nullptr);
             }
         }
-    } else if (warp == 9) {
-        // ------------------------------------------------------------ MMA issuer
-        // QK runs one key tile ahead of PV: QK(j + 1) is issued before PV(j), so the softmax of
-        // tile j overlaps it. With three S buffers, QK(j + 1) reuses the buffer of tile j - 2,
-        // whose PV was issued a whole step earlier, so the wait for it does not drain the pipe.
+    } else if (warp == 9 || warp == 11) {
+        // ------------------------------------------------------------ MMA issuers
+        // Two threads issue: warp 9 the QK MMAs, warp 11 the PV MMAs. The tensor pipe queues
+        // only about two MMAs behind an issuing thread, so a wait in a single issuer left the
+        // pipe idle; with two, one thread's waits are covered by the other's MMAs. Each thread's
+        // commits track its own MMAs, and every hazard between the two goes through a barrier:
+        // PV_j needs P_j (B_PREADY, after S_j and the softmax), QK_j reuses the S buffer of tile
+        // j - 3 only after PV_{j-3} (B_PVDONE), and the softmax rescales O only after PV_{j-1}.
+        // QK runs up to two tiles ahead of PV, as far as the K ring and the S buffers allow.
         if (lane == 0) {
             bool ok = wait_bar(bar(B_Q), 0, abort, ds);
-            auto issue_qk = [&](int j) -> bool {
-                const int st = j & 1, sb = j % kSBufs;
-                if (!wait_bar(bar(B_KFULL + st), (j >> 1) & 1, abort, ds)) return false;
-                if (j >= kSBufs && !wait_bar(bar(B_PVDONE + sb), ((j - kSBufs) / kSBufs) & 1, abort, ds)) return false;
-                tc_fence_after();
-                const uint32_t kb = sbase + OFF_K + st * 3 * kPanel;
+            if (warp == 9) {
+                for (int j = 0; j < n_tiles && ok; ++j) {
+                    const int st = j & 1, sb = j % kSBufs;
+                    if (!(ok = wait_bar(bar(B_KFULL + st), (j >> 1) & 1, abort, ds))) break;
+                    if (j >= kSBufs &&
+                        !(ok = wait_bar(bar(B_PVDONE + sb), ((j - kSBufs) / kSBufs) & 1, abort, ds)))
+                        break;
+                    tc_fence_after();
+                    const uint32_t kb = sbase + OFF_K + st * 3 * kPanel;
 #pragma unroll
-                for (int pn = 0; pn < 3; ++pn)
+                    for (int pn = 0; pn < 3; ++pn)
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(tmem + 128u * sb, smem_desc_sw128(sbase + OFF_Q + pn * kPanel + kk * 32, 16, 1024),
-                               smem_desc_sw128(kb + pn * kPanel + kk * 32, 16, 1024), kIdescQK, (pn | kk) ? 1u : 0u);
-                mma_commit(bar(B_KEMPTY + st));
-                mma_commit(bar(B_SFULL + sb));
-                return true;
-            };
-            auto issue_pv = [&](int i) -> bool {
-                const int st = i & 1, sb = i % kSBufs;
-                if (!wait_bar(bar(B_VFULL + st), (i >> 1) & 1, abort, ds)) return false;
-                if (!wait_bar(bar(B_PREADY + sb), (i / kSBufs) & 1, abort, ds)) return false;
-                tc_fence_after();
-                const uint32_t vb = sbase + OFF_V + st * 2 * kPanel;
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem + 128u * sb, smem_desc_sw128(sbase + OFF_Q + pn * kPanel + kk * 32, 16, 1024),
+                                   smem_desc_sw128(kb + pn * kPanel + kk * 32, 16, 1024), kIdescQK,
+                                   (pn | kk) ? 1u : 0u);
+                    mma_commit(bar(B_KEMPTY + st));
+                    mma_commit(bar(B_SFULL + sb));
+                }
+                mma_commit(bar(B_FINAL_QK));  // lands when every QK MMA issued above has completed
+                int ignore = 0;
+                wait_bar(bar(B_FINAL_QK), 0, &ignore, nullptr);
+            } else {
+                for (int i = 0; i < n_tiles && ok; ++i) {
+                    const int st = i & 1, sb = i % kSBufs;
+                    if (!(ok = wait_bar(bar(B_VFULL + st), (i >> 1) & 1, abort, ds))) break;
+                    if (!(ok = wait_bar(bar(B_PREADY + sb), (i / kSBufs) & 1, abort, ds))) break;
+                    tc_fence_after();  // P was written by the softmax warps' tcgen05.st
+                    const uint32_t vb = sbase + OFF_V + st * 2 * kPanel;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // 16 keys per step: 16 rows of V, 8 columns of P
-                    mma_ts(tmem + kOCol, tmem + 128u * sb + 8u * kk, smem_desc_sw128(vb + kk * 2048, kPanel, 1024),
-                           kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar(B_VEMPTY + st));
-                mma_commit(bar(B_PVDONE + sb));
-                return true;
-            };
-            if (ok) ok = issue_qk(0);
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                if (j + 1 < n_tiles && !(ok = issue_qk(j + 1))) break;
-                ok = issue_pv(j);
+                    for (int kk = 0; kk < 8; ++kk)  // 16 keys per step: 16 rows of V, 8 columns of P
+                        mma_ts(tmem + kOCol, tmem + 128u * sb + 8u * kk, smem_desc_sw128(vb + kk * 2048, kPanel, 1024),
+                               kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar(B_VEMPTY + st));
+                    mma_commit(bar(B_PVDONE + sb));
+                }
+                mma_commit(bar(B_FINAL));  // lands when every PV MMA issued above has completed
+                int ignore = 0;
+                wait_bar(bar(B_FINAL), 0, &ignore, nullptr);
             }
-            mma_commit(bar(B_FINAL));  // lands when every MMA issued above has completed
-            int ignore = 0;
-            wait_bar(bar(B_FINAL), 0, &ignore, nullptr);
         }
     } else {
         // ------------------------------------------------------------ softmax (warps 0-7)
