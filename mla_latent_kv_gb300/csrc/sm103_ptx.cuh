@@ -32,12 +32,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
-__device__ __forceinline__ uint32_t cluster_id_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -47,11 +41,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
 }
 
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
@@ -185,13 +174,6 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* gptr, uint32_t byte
                  : "memory");
 }
 
-// Prefetch one box of a tensor into L2 (no shared memory, no completion tracking).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void* map, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
 // TMA store of one box from this CTA's shared memory to global memory (elements outside the
 // tensor are not written), tracked by the issuing thread's bulk async-group.
 __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int32_t x, int32_t y, int32_t z) {
@@ -224,12 +206,6 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, uint32_t 
                      remote_dst),
                  "r"(local_src), "r"(bytes), "r"(remote_bar)
                  : "memory");
-}
-
-// Make this thread's generic-proxy shared-memory writes visible to the async proxy (tensor
-// core / TMA) of the CTA that owns the memory.
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_cta() {
