@@ -22,10 +22,8 @@
 //                     the group for 32 heads; fp32 online softmax with a lazily moved running
 //                     max (rescale only when a row's max grows by more than 2^8). P (bf16, in
 //                     the MMA's swizzled K-major layout) and the per-head rescale factors are
-//                     written to four one-page staging buffers. A copier warp sends each staged
-//                     page to CTA 1 with one bulk shared-to-shared copy (counted by bytes on CTA
-//                     1's barrier) once CTA 1's buffer for it is free, so the softmax warps never
-//                     wait on CTA 1 and the next group's softmax overlaps CTA 1's PV.
+//                     written to local staging buffers and sent to CTA 1 with one bulk
+//                     shared-to-shared copy per page (counted by bytes on CTA 1's barrier).
 //   CTA 1 ("output")  holds the 128 x 512 fp32 output accumulator -- all 512 TMEM columns of its
 //                     SM, the reason the work is split over two SMs -- streams the pages'
 //                     first 512 dims (mostly L2 hits), and accumulates O += P V per page with
@@ -57,8 +55,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 352;        // warp 0 TMA, warp 1 MMA, warps 2-9 softmax, warp 10 P copies (CTA 0) /
-                                     // 2-5 helpers, 2-9 epilogue, 10 idle (CTA 1)
+constexpr int kThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (CTA 0) / 2-5 helpers, 2-9 epilogue (CTA 1)
 constexpr int kPPG = 4;              // pages per group
 #ifndef MLA_PREFETCH_GROUPS
 #define MLA_PREFETCH_GROUPS 1
@@ -111,8 +108,7 @@ enum : int {
     B_PFULL = 24,       // [4] CTA1: P message landed (bulk copy tx)
     B_READY = 28,       // [4] CTA1: page ready for its PV MMA (128 helper threads)
     B_STATS = 32,       // CTA1: final row statistics written by CTA0 (one cluster-scope arrive)
-    B_STAGED = 33,      // [4] CTA0: a page's P message is in its staging buffer (128 softmax threads)
-    B_COUNT = 37
+    B_COUNT = 33
 };
 constexpr int OFF_TMEM = 512;
 constexpr int OFF_ABORT = 516;
@@ -213,7 +209,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t cnt = 1;
             if (i == B_SEMPTY || i == B_QREADY) cnt = 256;
             if (i >= B_READY && i < B_READY + kPBufs) cnt = 128;
-            if (i >= B_STAGED && i < B_STAGED + kPBufs) cnt = 128;
             bar_init(bar(i), cnt);
         }
         if (rank == 1)  // P buffers armed for their first message before CTA 0 can send one
@@ -338,22 +333,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     wait_bar(bar(B_SLOTEMPTY + m % kSlots), (m / kSlots) & 1, &dummy, nullptr);
                 }
             }
-        } else if (warp == 10) {
-            // ------------------------- P copies to CTA 1 -------------------------
-            // A page's message leaves once it is staged and CTA 1's buffer for it is free (the PV
-            // of the page kPBufs earlier is done). Waiting here rather than in a softmax warp
-            // lets the softmax of the next group run while CTA 1 is still busy.
-            if (lane == 0) {
-                const uint32_t pbuf_remote = map_to_rank(sbase + OFF_PB, 1);
-                const uint32_t pfull_remote = map_to_rank(bar(B_PFULL), 1);
-                for (int pg = 0; pg < npages; ++pg) {
-                    const int pbi = pg % kPBufs, u = pg / kPBufs;
-                    if (!wait_bar(bar(B_STAGED + pbi), u & 1, abort, ds)) break;
-                    if (u > 0 && !wait_bar<true>(bar(B_PEMPTY + pbi), (u - 1) & 1, abort, ds)) break;
-                    bulk_copy_to_peer(pbuf_remote + pbi * kPBufStride, sbase + OFF_STAGE + pbi * kPBufStride,
-                                      kPMsgBytes, pfull_remote + 8u * pbi);
-                }
-            }
         } else {
             // ------------------------- softmax warps (256 threads) -------------------------
             const int half = (warp - 2) >> 2;            // pages 2 half, 2 half + 1 of each group
@@ -395,6 +374,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // token dominates; lt sums the unrounded P for the LSE. Each half keeps its own sums
             // (same running max); they are added at the end.
             float m_run = -CUDART_INF_F, l_run = 0.f, lt_run = 0.f;
+            const uint32_t pbuf_remote = map_to_rank(sbase + OFF_PB, 1);
+            const uint32_t pfull_remote = map_to_rank(bar(B_PFULL), 1);
             for (int gi = 0; gi < ngroups; ++gi) {
                 // No early exit from this loop: all 256 threads must pass the same named barriers
                 // (which cannot time out); after an abort the waits return at once and the work
@@ -458,8 +439,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 l_run *= alpha;
                 lt_run *= alpha;
-                // does any row of this group move its max (then CTA 1 rescales O first)
-                const bool any = named_bar_or(kBarOr, 256, resc && gi > 0);
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const int page = pg0 + q;
@@ -495,12 +474,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < 8; ++c)
                             *reinterpret_cast<uint4*>(sbuf + row * 128 + ((c ^ (row & 7)) << 4)) =
                                 make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                        // every row's alpha rides with the group's first page, and so does the flag
+                        // every row's alpha rides with the group's first page
                         if (half == 0 && q == 0) reinterpret_cast<float*>(sbuf + kPBytes)[row] = alpha;
-                        if (row == 0)
-                            *reinterpret_cast<uint32_t*>(sbuf + kPBytes + 512) = (half == 0 && q == 0 && any) ? 1u : 0u;
                         fence_proxy_async_cta();
-                        bar_arrive(bar(B_STAGED + stg));  // warp 10 copies it out once CTA 1 has room
+                    }
+                }
+                const bool any = named_bar_or(kBarOr, 256, resc && gi > 0);
+                if (tid == 64 && !*abort) {  // one thread ships the group's pages
+                    for (int q = 0; q < kPPG; ++q) {
+                        const int pg = kPPG * gi + q;
+                        if (pg >= npages) break;
+                        uint8_t* b = smem + OFF_STAGE + (pg % kPBufs) * kPBufStride;
+                        *reinterpret_cast<uint32_t*>(b + kPBytes + 512) = (q == 0 && any) ? 1u : 0u;
+                        fence_proxy_async_cta();
+                        const int pbi = pg % kPBufs, upb = pg / kPBufs;
+                        if (upb > 0 && !wait_bar<true>(bar(B_PEMPTY + pbi), (upb - 1) & 1, abort, ds)) break;
+                        bulk_copy_to_peer(pbuf_remote + pbi * kPBufStride, smem_addr(b), kPMsgBytes,
+                                          pfull_remote + 8u * pbi);
                     }
                 }
             }
@@ -592,8 +582,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     wait_bar(bar(B_VEMPTY + i % kVStages), (i / kVStages) & 1, &dummy, nullptr);
                 }
             }
-        } else if (warp == 10) {
-            // idle in this CTA
         } else {
             // ------------- helper warps 2-5: P / V arrival, rescale, tail zeroing -------------
             // ------------- warps 2-9: the epilogue (each warp set stages half of the panels) ----
