@@ -415,6 +415,58 @@ def test_cache_write_fp8_quantises_per_definition(kv_scale):
         assert np.all(np.abs(deq[~inside] / float(ks)) == 448.0)
 
 
+def _torch_e4m3(v):
+    """float8_e4m3fn codes of binary32 values, saturated to +-448 first (torch maps overflow to NaN)."""
+    v = np.clip(np.asarray(v, np.float32), np.float32(-448.0), np.float32(448.0))
+    return torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _reciprocal_vs_quotient_values(s):
+    """Every positive finite bf16 value x whose e4m3 code differs between the binary32 product
+    x * (1 / s) and the binary32 quotient x / s (both within +-448)."""
+    x = (np.arange(1, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+    with np.errstate(over="ignore"):
+        mul = x * (np.float32(1.0) / s)
+        div = x / s
+    keep = (np.abs(mul) <= 448) & (np.abs(div) <= 448)
+    x, mul, div = x[keep], mul[keep], div[keep]
+    return x[_torch_e4m3(mul) != _torch_e4m3(div)]
+
+
+@pytest.mark.parametrize("per_token", [False, True])
+def test_cache_write_fp8_multiplies_by_the_reciprocal_scale(per_token):
+    """The quantising write stores e4m3(x * (1 / s)), both steps rounded in binary32: the page's
+    cache-write section describes the FP8 write as a multiplication by the scale factor (skipped
+    when the scale is exactly 1), and with the stored scale s defined by dequant = code * s that
+    factor is 1 / s. The expected bytes come from torch's float8_e4m3fn conversion of a numpy
+    binary32 product, and the inputs are values for which dividing by s instead gives another
+    code, so a writer that divides fails here."""
+    s = np.float32(7.0)  # 1/7 is inexact in binary32
+    vals = _reciprocal_vs_quotient_values(s)
+    assert len(vals) >= 16
+    row = np.zeros(576, np.float32)
+    row[: len(vals)] = vals[:575]
+    row[288: 288 + len(vals)] = -vals[:288]         # the negative side too
+    kv_scale = 0.0
+    if per_token:
+        row[575] = 3136.0                           # amax: 3136 / 448 = 7 exactly
+        assert np.float32(np.float32(3136.0) / np.float32(448.0)) == s
+    else:
+        kv_scale = float(s)
+    bits = mi.to_bf16_bits(row)
+    assert np.array_equal(oracle.widen_bf16(bits), row.astype(np.float64))  # the values are bf16
+    cache = np.zeros((1, 64 * 584), np.uint8)
+    slots = np.array([5], np.int64)
+    assert oracle.cache_write(bits[None, :512], bits[None, 512:], slots, oracle.KV_FP8, cache, 1,
+                              kv_scale=kv_scale) == 0
+    r = cache.reshape(64, 584)[5]
+    assert r[576:580].copy().view(np.float32)[0] == s and r[580:584].copy().view(np.float32)[0] == s
+    expect = _torch_e4m3(row * (np.float32(1.0) / s))
+    np.testing.assert_array_equal(r[:576], expect)
+    # the same inputs divided by s give other codes: the pin tells the two readings apart
+    assert np.count_nonzero(_torch_e4m3(row / s) != expect) >= 16
+
+
 # ----------------------------------------------------------------------------- variable-length query rows
 def test_varlen_equals_uniform_and_per_request_runs():
     """Packed rows with equal query lengths are the uniform batch; a request's rows in a mixed
