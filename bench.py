@@ -286,17 +286,14 @@ def run_ours(args):
     flush = torch.empty(args.flush_mb * (1 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(d0=None, d1=None):
-        # An event recorded between two kernels stops the second from starting early
-        # (programmatic dependent launch), so the decode call is bracketed only when asked.
-        mla.absorb_q(q_nope, q_pe, w_uk_t, out=q, stream=stream)
-        if d0 is not None:
-            d0.record(stream)
+    def decode_call():
         mla.decode(q.view(B, Sq, H, mi.D), cache, bt, sl, max_len, c["scale"], kv_dtype=c["kv"], num_splits=S,
                    workspace=ws, o_latent=o_lat, lse=lse, dev_status=status, stream=stream,
                    num_blocks=c["num_blocks"])
-        if d1 is not None:
-            d1.record(stream)
+
+    def step():
+        mla.absorb_q(q_nope, q_pe, w_uk_t, out=q, stream=stream)
+        decode_call()
         mla.out_proj(o_lat.view(T, H, mi.L), w_uv, out=o, stream=stream)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
@@ -305,8 +302,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
 
     K = args.steps
-    starts, ends, dstarts, dends = [ev() for _ in range(K)], [ev() for _ in range(K)], \
-        [ev() for _ in range(K)], [ev() for _ in range(K)]
+    starts, ends = [ev() for _ in range(K)], [ev() for _ in range(K)]
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -317,22 +313,27 @@ def run_ours(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    dec_every = 8  # decode bracketed by events on every 8th timed step (for the roofline)
     for k in range(K):
         flush.zero_()  # evict L2 between steps (outside the timed events)
         starts[k].record(stream)
-        if k % dec_every == 0:
-            step(dstarts[k], dends[k])
-        else:
-            step()
+        step()
         ends[k].record(stream)
+    torch.cuda.synchronize(dev)
+    # Decode alone, for the roofline: a loop of its own, whatever --steps is. Each launch follows
+    # an L2 flush and is bracketed by events on the launching stream; the median is reported.
+    n_dec = max(50, min(K, 200))
+    dec0, dec1 = [ev() for _ in range(n_dec)], [ev() for _ in range(n_dec)]
+    for k in range(n_dec):
+        flush.zero_()
+        dec0[k].record(stream)
+        decode_call()
+        dec1[k].record(stream)
     torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
     clocks = sampler.stop()
     step_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K
-    dec_idx = range(0, K, dec_every)
-    dec_ms = sum(dstarts[k].elapsed_time(dends[k]) for k in dec_idx) / len(dec_idx)
+    dec_ms = statistics.median(a.elapsed_time(b) for a, b in zip(dec0, dec1))
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     # ---------------- end to end through the public API with host buffers
@@ -435,7 +436,7 @@ def run_ours(args):
                "sample": f"{what}, absorbed fp64 route (decode only), {dt:.1f} s, "
                          f"scaled by H={H} items per token"}
     tokens = T * world
-    launches_per_step = 3 + (1 if S > 1 else 0)
+    launches_per_step = 3 + (1 if (S > 1 or S == -2) else 0) + (1 if S == -2 else 0)  # + merge, + plan
     line = {"metric": METRIC, "value": tokens / (step_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -443,7 +444,8 @@ def run_ours(args):
                        "kv_dtype": "fp8" if c["kv"] == mi.KV_FP8 else "bf16", "num_splits": S,
                        "o_dtype": args.o_dtype,
                        "l2": f"KV {kv_bytes / 1e6:.0f} MB > L2, plus a {args.flush_mb} MB L2 flush between steps",
-                       "decode_timing": "CUDA events around mla_decode on every 8th timed step",
+                       "decode_timing": f"median of {n_dec} launches of mla_decode alone, each after an L2 flush and "
+                                        "bracketed by CUDA events on its stream",
                        "e2e_timing": "pinned host inputs copied in and the result copied out every step, two "
                                      "buffer sets so that copies overlap the next step's compute; run time / steps, "
                                      "no flush (KV > L2)",
@@ -452,7 +454,7 @@ def run_ours(args):
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step * K, "clocks": clocks}
+            "gpu_launches": launches_per_step * K + (launches_per_step - 2) * n_dec, "clocks": clocks}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
