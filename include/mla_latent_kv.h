@@ -307,7 +307,9 @@ mla_status mla_prefill(const void* q, const void* kv_c, int64_t kv_c_stride_t, c
  * mla_decode_workspace_bytes_kv exceeds that (most FP8-cache batches: the expanded pages live
  * in the same scratch) is refused with MLA_ERR_WORKSPACE_TOO_SMALL. The first call on a
  * device looks up the array's device address (once per device, with that device current); make
- * that first call before any stream capture. The size check comes before any launch. Nothing
+ * that first call before any stream capture. The address is reused while the device's context
+ * stays the same; after a device reset the next call looks it up again (and is then again a
+ * first call). The size check comes before any launch. Nothing
  * here calls cudaMalloc,
  * cudaFree or any allocating library routine. All calls share the array: calls whose kernels
  * overlap on the GPU (e.g. issued on different streams) race on it and must be serialised by

@@ -12,6 +12,8 @@
 // streams) race on it and must be serialised by the caller. Its contents persist from call to
 // call; nothing in it needs to start at zero, because every partial the merge reads is written
 // by the same call's decode kernel first.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -28,24 +30,59 @@ constexpr int kMaxDevices = 64;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_mutex;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+struct ScratchEntry {
+    unsigned long long ctx_id;  // unique id of the context the address belongs to (0: unknown)
+    void* addr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device. The first call on a device does
-// the lookup (which may load this file's device code onto that device); make that first call
-// before any stream capture starts. Later calls read the cached address.
+// Unique id of the calling thread's current CUDA context, or 0 when there is none or the driver
+// does not offer the query. The two driver entry points are fetched once through the runtime,
+// so the library keeps no link-time dependency on libcuda.
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    if (!g_ctx_current || !g_ctx_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of the scratch array in the current device's context. The first call on a
+// device does the lookup (which may load this file's device code onto that device); make that
+// first call before any stream capture. Later calls reuse the address while the device's
+// context stays the same; after a device reset (a new primary context, with a new copy of the
+// array) the next call looks the address up again.
 cudaError_t scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
+    const unsigned long long id = current_context_id();
+    if (g_scratch[dev].addr == nullptr || id == 0 || g_scratch[dev].ctx_id != id) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
+        g_scratch[dev].addr = p;
+        g_scratch[dev].ctx_id = current_context_id();  // the lookup makes the primary context current
     }
-    *out = g_scratch_addr[dev];
+    *out = g_scratch[dev].addr;
     return cudaSuccess;
 }
 
