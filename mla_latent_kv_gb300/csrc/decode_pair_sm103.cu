@@ -61,22 +61,20 @@ constexpr int kThreads = 384;  // 12 warps: 0 K/Q loads, 1 V loads, 2 QK MMAs (e
 constexpr int kWarpSoftmax0 = 4;
 constexpr int kPPB = 4;                    // pages per block (2 per CTA)
 constexpr int kBox = 64 * 128;             // one TMA box: 64 rows x 64 bf16 (8 KB)
-constexpr int kKSlots = 4;                 // K ring: one 64-dim panel of this CTA's 128 tokens
-constexpr int kKSlotBytes = 2 * kBox;
-constexpr int kVStages = 3;                // V ring: 64 tokens x this CTA's 128 dims of one half
+constexpr int kKSlots = 5;                 // K ring: one 64-dim panel of this CTA's 128 tokens (16 KB)
+                                           // and the same panel of this CTA's 64 heads of Q (8 KB)
+constexpr int kKSlotBytes = 3 * kBox;
+constexpr int kVStages = 4;                // V ring: 64 tokens x this CTA's 128 dims of one half
 constexpr int kVStageBytes = 2 * kBox;
-constexpr int kQPanels = 9;                // 576 dims of this CTA's 64 heads
+constexpr int kQPanels = 9;                // 576 dims in 64-dim panels
+constexpr int kPBufs = 1;                  // P^T buffers (the PV MMAs of block b - kPBufs free one)
 constexpr int kPBytes = 256 * 128;         // P^T: 256 tokens x 64 heads bf16
 constexpr int kPHalfBytes = kPBytes / 2;   // the part the other CTA writes
-#ifndef MLA_PAIR_PREFETCH_BLOCKS
-#define MLA_PAIR_PREFETCH_BLOCKS 1
-#endif
-constexpr int kPrefetchBlocks = MLA_PAIR_PREFETCH_BLOCKS;
 
 // shared memory (the same layout in both CTAs: pair MMAs read the same offsets in each)
-constexpr int OFF_TMEM = 256;
-constexpr int OFF_ABORT = 260;
-constexpr int OFF_FLAG = 264;      // u32 [2]: a head moved its max in this block (even CTA's PV issuer)
+constexpr int OFF_TMEM = 320;
+constexpr int OFF_ABORT = 324;
+constexpr int OFF_FLAG = 328;      // u32 [2]: a head moved its max in this block (even CTA's PV issuer)
 constexpr int OFF_INVL = 512;      // f32 [128]: 1 / l for the epilogue
 constexpr int OFF_REDMAX = 1024;   // f32 [4][128]: block maxima of each lane quarter
 constexpr int OFF_REDSUM = 3072;   // f32 [4][128][2]: block sums (bf16-rounded P, unrounded P)
@@ -84,31 +82,29 @@ constexpr int OFF_MUSE = 7168;     // f32 [128]: running max (log2 units) the bl
 constexpr int OFF_ALPHA = 7680;    // f32 [128]: rescale factor of the block
 constexpr int OFF_MAXIN = 8192;    // f32 [4][128]: the other CTA's block maxima (st.async)
 constexpr int OFF_LIN = 10240;     // f32 [128][2]: the other CTA's final sums (st.async)
-constexpr int OFF_Q = 11264;
-constexpr int OFF_K = OFF_Q + kQPanels * kBox;
+constexpr int OFF_K = 11264;
 constexpr int OFF_V = OFF_K + kKSlots * kKSlotBytes;
 constexpr int OFF_P = OFF_V + kVStages * kVStageBytes;
-constexpr int kSmemBytes = OFF_P + kPBytes;
+constexpr int kSmemBytes = OFF_P + kPBufs * kPBytes;
 static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
-static_assert(OFF_LIN + 128 * 8 <= OFF_Q && OFF_INVL + 512 <= OFF_REDMAX, "control area");
-static_assert(OFF_Q % 1024 == 0 && OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0,
+static_assert(OFF_LIN + 128 * 8 <= OFF_K && OFF_INVL + 512 <= OFF_REDMAX, "control area");
+static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0,
               "128-byte-swizzled tiles need 1024-byte alignment");
 
 enum : int {
-    B_QFULL = 0,     // even CTA: both CTAs' Q panels landed (TMA tx, pair form)
-    B_KFULL = 1,     // [4] even CTA: both CTAs' K panels of a ring slot landed
-    B_KEMPTY = 5,    // [4] both: the slot's QK MMAs completed (pair commit)
-    B_SFULL = 9,     // [2] both: S^T buffer written
-    B_SFREE = 11,    // [2] even CTA: S^T buffer read by the 16 softmax warps of the pair
-    B_VFULL = 13,    // [3] each CTA: its V stage landed (TMA tx)
-    B_VREADY = 16,   // [3] even CTA: the odd CTA's V stage ready (tail rows zeroed)
-    B_VEMPTY = 19,   // [3] both: the stage's PV MMAs completed
-    B_PREADY = 22,   // each CTA: its P^T buffer complete (local writers + the other CTA's st.async bytes)
-    B_PVDONE = 23,   // both: the block's PV MMAs completed (P^T free, O^T updated)
-    B_MAXFULL = 24,  // [4] each CTA: the other CTA's block maxima landed (st.async)
-    B_CORR = 28,     // even CTA: O^T rescaled by the 16 softmax warps of the pair
-    B_LFULL = 29,    // each CTA: the other CTA's final sums landed
-    B_COUNT = 30
+    B_KFULL = 0,                     // [kKSlots] even CTA: both CTAs' K and Q panels of a slot landed
+    B_KEMPTY = B_KFULL + kKSlots,    // [kKSlots] both: the slot's QK MMAs completed (pair commit)
+    B_SFULL = B_KEMPTY + kKSlots,    // [2] both: S^T buffer written
+    B_SFREE = B_SFULL + 2,           // [2] even CTA: S^T buffer read by the 16 softmax warps of the pair
+    B_VFULL = B_SFREE + 2,           // [kVStages] each CTA: its V stage landed (TMA tx)
+    B_VREADY = B_VFULL + kVStages,   // [kVStages] even CTA: the odd CTA's V stage ready (tail rows zeroed)
+    B_VEMPTY = B_VREADY + kVStages,  // [kVStages] both: the stage's PV MMAs completed
+    B_PREADY = B_VEMPTY + kVStages,  // [kPBufs] each CTA: its P^T buffer complete (local writers + st.async bytes)
+    B_PVDONE = B_PREADY + kPBufs,    // [kPBufs] both: the PV MMAs of the block that used P^T buffer i completed
+    B_MAXFULL = B_PVDONE + kPBufs,   // [4] each CTA: the other CTA's block maxima landed (st.async)
+    B_CORR = B_MAXFULL + 4,          // even CTA: O^T rescaled by the 16 softmax warps of the pair
+    B_LFULL = B_CORR + 1,            // each CTA: the other CTA's final sums landed
+    B_COUNT = B_LFULL + 1
 };
 static_assert(8 * B_COUNT <= OFF_TMEM, "barriers");
 
@@ -166,9 +162,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-struct MaxOp {
-    __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
-};
 struct AddOp {
     __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
 };
@@ -187,15 +180,15 @@ __device__ __forceinline__ void xstep(float* v, int lane, int bit, Op op) {
     }
 }
 
-// v[0 .. 32) of every lane (32 indices, each lane's value of them) reduced over the warp's 32
-// lanes; lane l ends with indices 2l and 2l + 1 in v[0] and v[1] (the caller did the first step,
-// 64 -> 32, with bit 16).
+// v[0 .. 32) of every lane (32 indices) reduced over the warp's 32 lanes: lane l ends with
+// index l in v[0].
 template <class Op>
-__device__ __forceinline__ void xreduce_rest(float* v, int lane, Op op) {
-    xstep<16>(v, lane, 8, op);
-    xstep<8>(v, lane, 4, op);
-    xstep<4>(v, lane, 2, op);
-    xstep<2>(v, lane, 1, op);
+__device__ __forceinline__ void xreduce32(float (&v)[32], int lane, Op op) {
+    xstep<16>(v, lane, 16, op);
+    xstep<8>(v, lane, 8, op);
+    xstep<4>(v, lane, 4, op);
+    xstep<2>(v, lane, 2, op);
+    xstep<1>(v, lane, 1, op);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -231,11 +224,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int i = 0; i < B_COUNT; ++i) {
             uint32_t cnt = 1;
             if (i == B_SFREE || i == B_SFREE + 1 || i == B_CORR) cnt = 16;
-            if (i == B_PREADY) cnt = lead ? 130 : 129;
+            if (i >= B_PREADY && i < B_PREADY + kPBufs) cnt = lead ? 130 : 129;
             bar_init(bar(i), cnt);
         }
         // first phases of the barriers that count the other CTA's st.async bytes
-        bar_arrive_expect_tx(bar(B_PREADY), kPHalfBytes);
+        for (int i = 0; i < kPBufs; ++i) bar_arrive_expect_tx(bar(B_PREADY + i), kPHalfBytes);
         for (int i = 0; i < 4; ++i) bar_arrive_expect_tx(bar(B_MAXFULL + i), 128 * 4);
         bar_arrive_expect_tx(bar(B_LFULL), 128 * 8);
         fence_barrier_init();
@@ -252,23 +245,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (tid == 0) griddep_launch_dependents();
 
     if (warp == 0) {
-        // ---------------- Q and K loads (both CTAs; completion counted in the even CTA) ----------------
+        // ---------------- K and Q panels (both CTAs; completion counted in the even CTA) ----------------
+        // Every ring slot takes one 64-dim panel of this CTA's two pages (K) and the same panel of
+        // this CTA's 64 heads of Q. Q is re-read for every block: it is small and stays in L2,
+        // and not keeping it resident leaves shared memory for deeper rings.
         if (lane == 0 && npages > 0) {
             tma_prefetch_desc(&q_map);
             tma_prefetch_desc(&kv_map);
-            const uint32_t qfull = map_to_rank(bar(B_QFULL), 0);
             const uint32_t kfull = map_to_rank(bar(B_KFULL), 0);
             const int oob = (int)(p.num_blocks * kPage);
-            auto prefetch_block = [&](int bb) {  // this CTA's two pages of block bb into L2
-                for (int i = 0; i < 2; ++i) {
-                    const int pg = kPPB * bb + 2 * (int)rank + i;
-                    if (pg >= npages) break;
-                    const int yr = page_row(p, g.b, g.page0 + pg);
-                    if (yr < oob) bulk_prefetch_l2(p.cache + (size_t)yr * kBf16RowBytes, kPage * kBf16RowBytes);
-                }
-            };
-            for (int bb = 0; bb < kPrefetchBlocks && bb < nblocks; ++bb) prefetch_block(bb);
-            bool q_issued = false, ok = true;
+            const int qy = g.r * p.H + 64 * (int)rank;
+            bool ok = true;
             int issued = 0;
             for (int b = 0; b < nblocks && ok; ++b) {
                 int y[2];
@@ -276,30 +263,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int pg = kPPB * b + 2 * (int)rank + i;
                     y[i] = pg < npages ? page_row(p, g.b, g.page0 + pg) : oob;
                 }
-                if (b + kPrefetchBlocks < nblocks && b > 0) prefetch_block(b + kPrefetchBlocks);
                 for (int pn = 0; pn < kQPanels; ++pn) {
                     const int m = kQPanels * b + pn, slot = m % kKSlots, k = m / kKSlots;
-                    if (!q_issued && m == 2) {  // Q: the preceding kernel's output
-                        griddep_wait();
-                        if (lead) bar_arrive_expect_tx(bar(B_QFULL), 2 * kQPanels * kBox);
-                        for (int qn = 0; qn < kQPanels; ++qn)
-                            tma_load_2d_pair(sbase + OFF_Q + qn * kBox, &q_map, qfull, qn * 64,
-                                             g.r * p.H + 64 * (int)rank);
-                        q_issued = true;
-                        if (b == 0 && kPrefetchBlocks < nblocks) prefetch_block(kPrefetchBlocks);
-                    }
                     if (k > 0 && !(ok = wait_bar<true>(bar(B_KEMPTY + slot), (k - 1) & 1, abort, ds))) break;
                     if (lead) bar_arrive_expect_tx(bar(B_KFULL + slot), 2 * kKSlotBytes);
                     const uint32_t dst = sbase + OFF_K + slot * kKSlotBytes;
                     for (int i = 0; i < 2; ++i) tma_load_2d_pair(dst + i * kBox, &kv_map, kfull + 8u * slot, pn * 64, y[i]);
+                    if (m == kKSlots - 1) {
+                        // Q is the preceding kernel's output: the first slots' K panels went out
+                        // before the wait, their Q panels after it
+                        griddep_wait();
+                        for (int mm = 0; mm < kKSlots; ++mm)
+                            tma_load_2d_pair(sbase + OFF_K + mm * kKSlotBytes + 2 * kBox, &q_map, kfull + 8u * mm, mm * 64, qy);
+                    } else if (m >= kKSlots) {
+                        tma_load_2d_pair(dst + 2 * kBox, &q_map, kfull + 8u * slot, pn * 64, qy);
+                    }
                     ++issued;
                 }
             }
             if (*abort && lead) {  // let the copies in flight land before the pair can exit
-                volatile int dummy = 0;
-                if (q_issued) wait_bar<true>(bar(B_QFULL), 0, &dummy, nullptr);
                 for (int m = (issued > kKSlots ? issued - kKSlots : 0); m < issued; ++m) {
-                    dummy = 0;
+                    volatile int dummy = 0;
                     wait_bar<true>(bar(B_KFULL + m % kKSlots), (m / kKSlots) & 1, &dummy, nullptr);
                 }
             }
@@ -333,7 +317,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // ---------------- QK^T MMAs: S^T[token][head] per block, double-buffered ----------------
             if (lane == 0 && npages > 0) {
                 int done = 0;
-                bool ok = wait_bar<true>(bar(B_QFULL), 0, abort, ds);
+                bool ok = true;
                 for (int b = 0; b < nblocks && ok; ++b) {
                     const int sb = b & 1;
                     if (b >= 2) {  // the 16 softmax warps of the pair have read S^T of block b - 2
@@ -345,7 +329,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const int m = kQPanels * b + pn, slot = m % kKSlots;
                         if (!(ok = wait_bar<true>(bar(B_KFULL + slot), (m / kKSlots) & 1, abort, ds))) break;
                         const uint32_t kb = sbase + OFF_K + slot * kKSlotBytes;
-                        const uint32_t qb = sbase + OFF_Q + pn * kBox;
+                        const uint32_t qb = kb + 2 * kBox;
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             mma_pair_ss(d, smem_desc_sw128(kb + 32 * j, 16, 1024), smem_desc_sw128(qb + 32 * j, 16, 1024),
@@ -364,9 +348,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else if (lane == 0 && npages > 0) {
             // ---------------- odd CTA: its P^T buffer is complete -> tell the even CTA ----------------
             for (int b = 0; b < nblocks; ++b) {
-                if (!wait_bar<true>(bar(B_PREADY), b & 1, abort, ds)) break;
-                bar_arrive_remote(bar(B_PREADY), 0);
-                if (b + 1 < nblocks) bar_arrive_expect_tx(bar(B_PREADY), kPHalfBytes);
+                const int pbi = b % kPBufs;
+                if (!wait_bar<true>(bar(B_PREADY + pbi), (b / kPBufs) & 1, abort, ds)) break;
+                bar_arrive_remote(bar(B_PREADY + pbi), 0);
+                if (b + kPBufs < nblocks) bar_arrive_expect_tx(bar(B_PREADY + pbi), kPHalfBytes);
             }
         }
     } else if (warp == 3) {
@@ -398,8 +383,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int vi = 0, ncorr = 0;
             bool ok = true;
             for (int b = 0; b < nblocks && ok; ++b) {
-                if (!(ok = warp_wait<true>(bar(B_PREADY), b & 1, abort, ds))) break;
-                if (lane == 0 && b + 1 < nblocks) bar_arrive_expect_tx(bar(B_PREADY), kPHalfBytes);
+                const int pbi = b % kPBufs;
+                if (!(ok = warp_wait<true>(bar(B_PREADY + pbi), (b / kPBufs) & 1, abort, ds))) break;
+                if (lane == 0 && b + kPBufs < nblocks) bar_arrive_expect_tx(bar(B_PREADY + pbi), kPHalfBytes);
                 if (*reinterpret_cast<volatile uint32_t*>(smem + OFF_FLAG + 4 * (b & 1))) {
                     if (!(ok = warp_wait<true>(bar(B_CORR), ncorr & 1, abort, ds))) break;
                     ++ncorr;
@@ -416,7 +402,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (lane == 0) {
                             tc_fence_after();
                             const uint32_t vb = sbase + OFF_V + st * kVStageBytes;
-                            const uint32_t pb = sbase + OFF_P + pg * 64 * 128;
+                            const uint32_t pb = sbase + OFF_P + pbi * kPBytes + pg * 64 * 128;
                             for (int kk = 0; kk < nk; ++kk)
                                 mma_pair_ss(tmem + kColO + 128u * a, smem_desc_sw128(vb + kk * 2048, kBox, 1024),
                                             smem_desc_sw128(pb + kk * 2048, kBox, 1024), kIdescPV,
@@ -427,7 +413,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         ++vi;
                     }
                 }
-                if (ok && lane == 0) mma_pair_commit(bar(B_PVDONE));
+                if (ok && lane == 0) mma_pair_commit(bar(B_PVDONE + pbi));
                 __syncwarp();
             }
             if (lane == 0) {
@@ -458,58 +444,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t peer_maxin = map_to_rank(sbase + OFF_MAXIN, peer);
         const uint32_t peer_maxfull = map_to_rank(bar(B_MAXFULL), peer);
         const bool p_local = ch == (int)rank;  // this thread's 64 heads are held by this CTA
-        const uint32_t p_dst = p_local ? sbase + OFF_P + prow * 128 : map_to_rank(sbase + OFF_P + prow * 128, peer);
+        const uint32_t p_row = p_local ? sbase + OFF_P + prow * 128 : map_to_rank(sbase + OFF_P + prow * 128, peer);
         const uint32_t peer_pready = map_to_rank(bar(B_PREADY), peer);
 
         for (int b = 0; b < nblocks; ++b) {
             // No early exit from this loop: all 256 threads must pass the same named barriers
             // (which cannot time out); after an abort the waits return at once and the work is
-            // skipped.
+            // skipped. S^T stays in tensor memory for the whole block: each 32-head half is read
+            // twice (for the max, then for P), which keeps 32 scores per thread in registers.
             const int sb = b & 1;
-            float s[64];
             const bool okS = warp_wait<true>(bar(B_SFULL + sb), (b >> 1) & 1, abort, ds);
-            if (okS) {
-                tc_fence_after();
-                uint32_t v0[32], v1[32];
-                tmem_ld32(tmem + lane_base + 128u * sb + 64u * ch, v0);
-                tmem_ld32(tmem + lane_base + 128u * sb + 64u * ch + 32u, v1);
-                tmem_wait_ld();
-                tc_fence_before();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    s[j] = __uint_as_float(v0[j]);
-                    s[32 + j] = __uint_as_float(v1[j]);
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    if (lead)
-                        bar_arrive(bar(B_SFREE + sb));
-                    else
-                        bar_arrive_remote(bar(B_SFREE + sb), 0);
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 64; ++j) s[j] = -CUDART_INF_F;
-            }
-            // tokens past the unit's last visible one: -inf; heads past H: 0 (kept finite)
+            if (okS) tc_fence_after();
             const bool tvalid = kPPB * kPage * b + tl + 128 * (int)rank < ntok;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                if (64 * ch + j >= p.H) s[j] = 0.f;
-                if (!tvalid) s[j] = -CUDART_INF_F;
-            }
-            // block max of each head over this CTA's 128 tokens
-            {
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const bool up = (lane & 16) != 0;
-                    const float send = up ? s[i] : s[i + 32];
-                    const float keep = up ? s[i + 32] : s[i];
-                    v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+            // masking is needed only in a unit's last, partial block and when H < 128
+            const bool masked = kPPB * kPage * (b + 1) > ntok || p.H < 128 || !okS;
+            // scores of heads 64 ch + 32 k .. + 31: -inf past the unit's last token, 0 past H
+            auto load_half = [&](int k, float (&x)[32]) {
+                uint32_t v[32];
+                if (okS) {
+                    tmem_ld32(tmem + lane_base + 128u * sb + 64u * ch + 32u * k, v);
+                    tmem_wait_ld();
                 }
-                xreduce_rest(v, lane, MaxOp());
-                *reinterpret_cast<float2*>(redmax + wq * 128 + 64 * ch + 2 * lane) = make_float2(v[0], v[1]);
+                if (!masked) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        float f = okS ? __uint_as_float(v[j]) : -CUDART_INF_F;
+                        if (64 * ch + 32 * k + j >= p.H) f = 0.f;
+                        x[j] = tvalid ? f : -CUDART_INF_F;
+                    }
+                }
+            };
+            // block max of each head over this CTA's 128 tokens; lane l ends with head 64 ch + 32 k + l
+#pragma unroll 1
+            for (int k = 0; k < 2; ++k) {
+                float x[32];
+                load_half(k, x);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = redux_max(x[j]);  // the same in every lane
+                if (lane == 0) {
+                    float4* dst = reinterpret_cast<float4*>(redmax + wq * 128 + 64 * ch + 32 * k);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) dst[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+                }
             }
             named_bar(kBarA, 256);
             bool moved = false;
@@ -534,40 +513,82 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             const bool any = named_bar_or(kBarB, 256, moved);
             if (stid == 0 && lead) *reinterpret_cast<volatile uint32_t*>(smem + OFF_FLAG + 4 * (b & 1)) = any ? 1u : 0u;
-            // P = exp2(S * scale * log2e - m), rounded once to bf16 for the MMA, written 16 bytes
-            // (8 heads) at a time as this token's P^T row in the CTA that holds the heads
-            if (b > 0) warp_wait<true>(bar(B_PVDONE), (b - 1) & 1, abort, ds);  // P^T free again
+            // P = exp2(S * scale * log2e - m), rounded once to bf16 for the MMA and written 16 bytes
+            // (8 heads) at a time as this token's P^T row in the CTA that holds the heads; the
+            // block's two sums per head (bf16-rounded P, unrounded P) reduced over the lanes
+            const int pbi = b % kPBufs;
+            if (b >= kPBufs)  // P^T buffer free again: the PV MMAs of block b - 2 completed
+                warp_wait<true>(bar(B_PVDONE + pbi), ((b - kPBufs) / kPBufs) & 1, abort, ds);
             const bool wr = okS && !*abort;
+#pragma unroll 1
+            for (int k = 0; k < 2; ++k) {
+                float x[32];
+                uint32_t pw[16];  // the bf16 P of the 32 heads, two to a word
+                load_half(k, x);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 ma = *reinterpret_cast<const float4*>(muse + 64 * ch + 8 * c);
-                const float4 mb = *reinterpret_cast<const float4*>(muse + 64 * ch + 8 * c + 4);
-                float* x = s + 8 * c;
-                x[0] = fast_exp2(fmaf(x[0], sl2, -ma.x));
-                x[1] = fast_exp2(fmaf(x[1], sl2, -ma.y));
-                x[2] = fast_exp2(fmaf(x[2], sl2, -ma.z));
-                x[3] = fast_exp2(fmaf(x[3], sl2, -ma.w));
-                x[4] = fast_exp2(fmaf(x[4], sl2, -mb.x));
-                x[5] = fast_exp2(fmaf(x[5], sl2, -mb.y));
-                x[6] = fast_exp2(fmaf(x[6], sl2, -mb.z));
-                x[7] = fast_exp2(fmaf(x[7], sl2, -mb.w));
-                const uint4 w = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                                           pack_bf16x2(x[6], x[7]));
-                const uint32_t off = (uint32_t)((c ^ (prow & 7)) << 4);
-                if (wr) {
-                    if (p_local)
-                        *reinterpret_cast<uint4*>(smem + OFF_P + prow * 128 + off) = w;
-                    else
-                        st_async_v4(p_dst + off, w, peer_pready);
+                for (int c = 0; c < 4; ++c) {
+                    const float4 ma = *reinterpret_cast<const float4*>(muse + 64 * ch + 32 * k + 8 * c);
+                    const float4 mb = *reinterpret_cast<const float4*>(muse + 64 * ch + 32 * k + 8 * c + 4);
+                    float* y = x + 8 * c;
+                    y[0] = fast_exp2(fmaf(y[0], sl2, -ma.x));
+                    y[1] = fast_exp2(fmaf(y[1], sl2, -ma.y));
+                    y[2] = fast_exp2(fmaf(y[2], sl2, -ma.z));
+                    y[3] = fast_exp2(fmaf(y[3], sl2, -ma.w));
+                    y[4] = fast_exp2(fmaf(y[4], sl2, -mb.x));
+                    y[5] = fast_exp2(fmaf(y[5], sl2, -mb.y));
+                    y[6] = fast_exp2(fmaf(y[6], sl2, -mb.z));
+                    y[7] = fast_exp2(fmaf(y[7], sl2, -mb.w));
+                    pw[4 * c] = pack_bf16x2(y[0], y[1]);
+                    pw[4 * c + 1] = pack_bf16x2(y[2], y[3]);
+                    pw[4 * c + 2] = pack_bf16x2(y[4], y[5]);
+                    pw[4 * c + 3] = pack_bf16x2(y[6], y[7]);
+                    const uint4 w = make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+                    const int cc = 4 * k + c;
+                    const uint32_t off = (uint32_t)((cc ^ (prow & 7)) << 4);
+                    if (wr) {
+                        if (p_local)
+                            *reinterpret_cast<uint4*>(smem + OFF_P + pbi * kPBytes + prow * 128 + off) = w;
+                        else
+                            st_async_v4(p_row + pbi * kPBytes + off, w, peer_pready + 8u * pbi);
+                    }
                 }
+                // rounded sum: the first step moves two bf16 values per shuffle
+                float r[16];
+                {
+                    const bool up = (lane & 16) != 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t send = up ? pw[i] : pw[i + 8];
+                        const uint32_t keep = up ? pw[i + 8] : pw[i];
+                        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
+                        r[2 * i] = bf16_lo_f(keep) + bf16_lo_f(recv);
+                        r[2 * i + 1] = bf16_hi_f(keep) + bf16_hi_f(recv);
+                    }
+                }
+                xstep<8>(r, lane, 8, AddOp());
+                xstep<4>(r, lane, 4, AddOp());
+                xstep<2>(r, lane, 2, AddOp());
+                xstep<1>(r, lane, 1, AddOp());
+                xreduce32(x, lane, AddOp());
+                *reinterpret_cast<float2*>(redsum + 2 * (wq * 128 + 64 * ch + 32 * k + lane)) = make_float2(r[0], x[0]);
+            }
+            // S^T of this block has been read for the last time
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && okS) {
+                if (lead)
+                    bar_arrive(bar(B_SFREE + sb));
+                else
+                    bar_arrive_remote(bar(B_SFREE + sb), 0);
             }
             if (wr && p_local) {
                 fence_proxy_async_cta();
-                bar_arrive(bar(B_PREADY));
+                bar_arrive(bar(B_PREADY + pbi));
             }
             // a head moved its max: scale its O^T column (this warp's quarter of the lanes, its
             // accumulator) before the block's PV MMAs
             if (any && okS && !*abort) {
+                warp_wait<true>(bar(B_PVDONE + (b - 1) % kPBufs), ((b - 1) / kPBufs) & 1, abort, ds);
                 tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
@@ -589,33 +610,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         bar_arrive_remote(bar(B_CORR), 0);
                 }
             }
-            // the block's two sums per head over this CTA's tokens, one after the other: the
-            // bf16-rounded P (recomputed from s) and the unrounded P; lane l ends with heads
-            // 64 ch + 2l and + 1
-            float vr[32];
-            {
-                const bool up = (lane & 16) != 0;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const uint32_t w = pack_bf16x2(s[i], s[i + 32]);
-                    const float a0 = bf16_lo_f(w), a1 = bf16_hi_f(w);
-                    const float send = up ? a0 : a1;
-                    const float keep = up ? a1 : a0;
-                    vr[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-                }
-                xreduce_rest(vr, lane, AddOp());
-                float vu[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float send = up ? s[i] : s[i + 32];
-                    const float keep = up ? s[i + 32] : s[i];
-                    vu[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-                }
-                xreduce_rest(vu, lane, AddOp());
-                vr[2] = vu[0];
-                vr[3] = vu[1];
-            }
-            *reinterpret_cast<float4*>(redsum + 2 * (wq * 128 + 64 * ch + 2 * lane)) = make_float4(vr[0], vr[2], vr[1], vr[3]);
             named_bar(kBarC, 256);
             if (head_thr) {
                 const float2 s0 = *reinterpret_cast<const float2*>(redsum + 2 * hh);
@@ -653,7 +647,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
         }
         named_bar(kBarA, 256);
-        bool use_o = nblocks > 0 && warp_wait<true>(bar(B_PVDONE), (nblocks - 1) & 1, abort, ds);
+        bool use_o = nblocks > 0 &&
+                     warp_wait<true>(bar(B_PVDONE + (nblocks - 1) % kPBufs), ((nblocks - 1) / kPBufs) & 1, abort, ds);
         use_o = use_o && !*abort;
         tc_fence_after();
         griddep_wait();

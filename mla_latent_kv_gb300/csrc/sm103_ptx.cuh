@@ -399,6 +399,13 @@ __device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
     asm volatile("barrier.cta.sync.aligned %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Maximum of x over the 32 lanes of the warp; every lane receives it.
+__device__ __forceinline__ float redux_max(float x) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // Hardware base-2 exponential (MUFU), flushing subnormal results to zero; exp2(-inf) = 0.
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
