@@ -136,7 +136,6 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 mla_status set_error(mla_status st, const char* fmt, ...);
 
 cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s);
-cudaError_t launch_decode_pair_sm103(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_fp8_expand(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_plan(const DecodeArgs& a, int pairs, cudaStream_t s);

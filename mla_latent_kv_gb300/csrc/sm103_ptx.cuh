@@ -281,58 +281,6 @@ __device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_
         : "memory");
 }
 
-// ------------------------------------------------------------------------------------------
-// tcgen05 in pair mode (cta_group::2): one MMA spans the two CTAs of a cluster pair. Its M rows
-// are split between the CTAs (rows [0, M/2) in the even CTA's tensor memory and shared memory,
-// [M/2, M) in the odd CTA's), its B operand's N rows likewise (each CTA holds N/2 of them at the
-// same shared-memory offset), and each CTA's tensor memory receives its M/2 rows x all N columns.
-// Only the even CTA issues the MMAs and commits; the allocation is made by one warp of each CTA.
-// A kernel that uses pair mode uses it for all of its tcgen05 allocation, MMA and commit
-// instructions.
-// ------------------------------------------------------------------------------------------
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {  // whole warp, both CTAs
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish_pair() {  // whole warp
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {  // whole warp, both CTAs
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// D[tmem] (+)= A[smem desc] x B[smem desc] over the pair (issued by the even CTA).
-__device__ __forceinline__ void mma_pair_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive once on the barrier at offset `bar` of both CTAs of the pair when every pair-mode
-// tcgen05 operation issued so far by this thread has completed.
-__device__ __forceinline__ void mma_pair_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"((uint16_t)0x3)
-        : "memory");
-}
-
-// TMA tile load into this CTA's shared memory whose completion (bytes) is counted on a barrier
-// of either CTA of the pair: `bar` is a shared::cluster address (see map_to_rank).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* map, uint32_t bar, int32_t x, int32_t y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-
 // Asynchronous stores into the other CTA's shared memory: `remote` and `remote_bar` are
 // shared::cluster addresses in the same CTA; the stored bytes are counted (complete_tx) on that
 // barrier.
@@ -397,13 +345,6 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, boo
 
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
     asm volatile("barrier.cta.sync.aligned %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Maximum of x over the 32 lanes of the warp; every lane receives it.
-__device__ __forceinline__ float redux_max(float x) {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
-    return r;
 }
 
 // Hardware base-2 exponential (MUFU), flushing subnormal results to zero; exp2(-inf) = 0.
