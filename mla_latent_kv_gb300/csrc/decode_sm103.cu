@@ -12,25 +12,25 @@
 //
 //   CTA 0 ("scores")  Q: the 512 latent dims (128 heads x 512 bf16) are loaded once by TMA and
 //                     kept in tensor memory; the 64 rope dims stay in shared memory.
-//                     K: a ring of four 32 KB slots, one slot = one 64-dim panel of a group's
-//                     four pages (256 rows, 128-byte swizzle), refilled panel by panel as the
-//                     MMAs release them.
+//                     K: a ring of six 32 KB slots, one slot = one 64-dim panel of a group's
+//                     four pages (256 rows, 128-byte swizzle), refilled panel by panel by TMA as
+//                     the MMAs release them.
 //                     S = Q K^T per group: 36 tcgen05.mma of M=128 heads x N=256 tokens x K=16
 //                     (32 with A from TMEM, 4 with A = rope dims from shared memory) into a
 //                     256-column TMEM buffer.
 //                     Softmax: eight warps, two per TMEM lane quarter, each owning two pages of
 //                     the group for 32 heads; fp32 online softmax with a lazily moved running
-//                     max (rescale only when a row's max grows by more than 2^8). P (bf16, in
-//                     the MMA's swizzled K-major layout) and the per-head rescale factors are
-//                     written to local staging buffers and sent to CTA 1 with one bulk
-//                     shared-to-shared copy per page (counted by bytes on CTA 1's barrier).
+//                     max (rescale only when a row's max grows by more than 2^8). Each thread
+//                     stores its head's P row (bf16, in the MMA's swizzled K-major layout) and
+//                     rescale factor straight into CTA 1's P buffer for the page with st.async,
+//                     whose bytes are counted on CTA 1's barrier for that buffer.
 //   CTA 1 ("output")  holds the 128 x 512 fp32 output accumulator -- all 512 TMEM columns of its
 //                     SM, the reason the work is split over two SMs -- streams the pages'
 //                     first 512 dims (mostly L2 hits), and accumulates O += P V per page with
 //                     tcgen05.mma (M=128, N=2x256, K=64; V read as an MN-major operand straight
-//                     from the TMA tile). Its MMA thread waits on a single barrier per page; four
-//                     helper warps do everything else: wait for P and V, hand the staging buffer
-//                     back, rescale O, zero the V rows past the last token, and the epilogue.
+//                     from the TMA tile). Its MMA thread waits for P, the helpers and V; four
+//                     helper warps re-arm the P buffers, rescale O, zero the V rows past the
+//                     last token, and (with four more warps) run the epilogue.
 // Per page the pair issues exactly the algorithm's 2*128*64*(576+512) flops.
 //
 // Rows past the split's last visible token are masked by index (S = -inf) and, in the last
@@ -57,59 +57,58 @@ using namespace ptx;
 
 constexpr int kThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (CTA 0) / 2-5 helpers, 2-9 epilogue (CTA 1)
 constexpr int kPPG = 4;              // pages per group
-#ifndef MLA_PREFETCH_GROUPS
-#define MLA_PREFETCH_GROUPS 1
-#endif
-constexpr int kPrefetchGroups = MLA_PREFETCH_GROUPS;  // L2 prefetch distance in groups
-constexpr int kSlots = 4;            // CTA 0 K ring slots
+constexpr int kSlots = 6;            // CTA 0 K ring slots (32 KB each)
 constexpr int kPageBox = 64 * 128;   // one page's rows of one 64-dim panel (8 KB)
 constexpr int kSlotBytes = kPPG * kPageBox;  // 32 KB
 constexpr int kQPanelBytes = 128 * 128;      // 128 heads x 64 dims of Q (16 KB)
-constexpr int kPBufs = 4;            // P buffers: CTA 0 staging and CTA 1 receive (one page each)
-constexpr int kVStages = 2;          // CTA 1 V ring (one page each)
-constexpr int kVStageBytes = 8 * kPageBox;      // 65,536
+constexpr int kPBufs = 5;            // CTA 1 P buffers (one page each): P arrives up to 5 pages ahead
+constexpr int kVStages = 2;          // CTA 1 V ring stages of kVRows tokens x 512 dims
+constexpr int kVRows = 64;           // one page per V stage
+constexpr int kVPerPage = kPage / kVRows;        // V stages per page
+constexpr int kVBox = kVRows * 128;             // one 64-dim panel of a V stage (8 KB)
+constexpr int kVStageBytes = 8 * kVBox;         // 64 KB
 constexpr int kPBytes = 128 * 128;              // P page: 128 heads x 64 tokens bf16
-constexpr int kPMsgBytes = kPBytes + 512 + 16;  // P + alpha[128] + flag word: one bulk copy
+constexpr int kPMsgBytes = kPBytes + 512 + 4;   // P + alpha[128] + flag word, stored by st.async
 constexpr int kPBufStride = 17 * 1024;
 constexpr int kCtrlBytes = 4096;
 // CTA 0 layout
 constexpr int OFF_QROPE = kCtrlBytes;                      // 16 KB
-constexpr int OFF_RING = OFF_QROPE + kQPanelBytes;         // 4 x 32 KB
-constexpr int OFF_STAGE = OFF_RING + kSlots * kSlotBytes;  // 4 x 17 KB
-constexpr int kSmem0 = OFF_STAGE + kPBufs * kPBufStride;
+constexpr int OFF_RING = OFF_QROPE + kQPanelBytes;         // 6 x 32 KB
+constexpr int kSmem0 = OFF_RING + kSlots * kSlotBytes;
 // CTA 1 layout
 constexpr int OFF_V = kCtrlBytes;
 constexpr int OFF_PB = OFF_V + kVStages * kVStageBytes;
 constexpr int kSmem1 = OFF_PB + kPBufs * kPBufStride;
 constexpr int kSmemBytes = kSmem0 > kSmem1 ? kSmem0 : kSmem1;
 static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
-static_assert(kPMsgBytes % 16 == 0 && kPMsgBytes <= kPBufStride, "P message");
-// Q's latent panels land outside ring slots 0 and 1 (so that the first K panels can load at
-// once): panels 0-3 in the P staging area, panels 4-7 in ring slots 2 and 3.
-static_assert(4 * kQPanelBytes <= kPBufs * kPBufStride && 4 * kQPanelBytes == 2 * kSlotBytes, "Q panel homes");
-static_assert(OFF_STAGE % 1024 == 0, "Q panels in the staging area keep the 128-byte swizzle alignment");
-__device__ __forceinline__ uint32_t q_panel_off(int pn) {
-    return pn < 4 ? OFF_STAGE + pn * kQPanelBytes : OFF_RING + 2 * kSlotBytes + (pn - 4) * kQPanelBytes;
-}
+static_assert(kPMsgBytes <= kPBufStride, "P message");
+// Q's latent panels land in ring slots 2-5, so that the first K panels can load into slots 0
+// and 1 at once.
+static_assert(8 * kQPanelBytes == 4 * kSlotBytes && kSlots >= 6, "Q panel homes");
+static_assert(OFF_RING % 1024 == 0 && OFF_PB % 1024 == 0 && kPBufStride % 1024 == 0 && kVBox % 1024 == 0,
+              "128-byte swizzled tiles need 1024-byte alignment");
+// the epilogue stages its output tiles over the V ring and the P buffers
+static_assert(OFF_V + 8 * 128 * 128 <= kSmem1, "epilogue tiles");
+__device__ __forceinline__ uint32_t q_panel_off(int pn) { return OFF_RING + 2 * kSlotBytes + pn * kQPanelBytes; }
 
 // Barrier slots (8 bytes each); one layout for both CTAs so that a multicast commit from CTA 1
 // lands on CTA 0's B_PEMPTY slots.
 enum : int {
-    B_SLOTFULL = 0,     // [4] CTA0: ring slot landed (TMA tx)
-    B_SLOTEMPTY = 4,    // [4] CTA0: ring slot consumed by the QK MMAs
-    B_SFULL = 8,        // CTA0: S ready
-    B_SEMPTY = 9,       // CTA0: S read into registers by the softmax warps (256)
-    B_QFULL = 10,       // CTA0: Q landed in shared memory (TMA tx)
-    B_QREADY = 11,      // CTA0: Q latent dims moved to TMEM, ring free for K (256)
-    B_STAGEFREE = 12,   // [4] CTA0: staging buffer copied out (arrive from CTA1)
-    B_PEMPTY = 16,      // [4] both CTAs: PV MMA of the page in P buffer b completed (multicast commit)
-    B_VFULL = 20,       // [2] CTA1: V stage landed
-    B_VEMPTY = 22,      // [2] CTA1: V stage consumed
-    B_PFULL = 24,       // [4] CTA1: P message landed (bulk copy tx)
-    B_READY = 28,       // [4] CTA1: page ready for its PV MMA (128 helper threads)
-    B_STATS = 32,       // CTA1: final row statistics written by CTA0 (one cluster-scope arrive)
-    B_COUNT = 33
+    B_SLOTFULL = 0,                    // [kSlots] CTA0: ring slot landed (TMA tx)
+    B_SLOTEMPTY = B_SLOTFULL + kSlots, // [kSlots] CTA0: ring slot consumed by the QK MMAs
+    B_SFULL = B_SLOTEMPTY + kSlots,    // CTA0: S ready
+    B_SEMPTY,                          // CTA0: S read into registers by the softmax warps (256)
+    B_QFULL,                           // CTA0: Q landed in shared memory (TMA tx)
+    B_QREADY,                          // CTA0: Q latent dims moved to TMEM, ring free for K (256)
+    B_PEMPTY,                          // [kPBufs] both CTAs: PV MMA of the page in P buffer b completed
+    B_VFULL = B_PEMPTY + kPBufs,       // [kVStages] CTA1: V stage landed
+    B_VEMPTY = B_VFULL + kVStages,     // [kVStages] CTA1: V stage consumed
+    B_PFULL = B_VEMPTY + kVStages,     // [kPBufs] CTA1: P message landed (st.async bytes from CTA0)
+    B_READY = B_PFULL + kPBufs,        // [kPBufs] CTA1: page ready for its PV MMA (128 helper threads)
+    B_STATS = B_READY + kPBufs,        // CTA1: final row statistics written by CTA0 (one cluster-scope arrive)
+    B_COUNT
 };
+static_assert(8 * B_COUNT <= 512, "barrier slots");
 constexpr int OFF_TMEM = 512;
 constexpr int OFF_ABORT = 516;
 constexpr int OFF_MX = 1024;       // CTA0: f32 [2][128] exchange between the two warp halves
@@ -178,7 +177,8 @@ __device__ __forceinline__ int valid_rows(const RowGeom& g, int page) {
 
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_sm103_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+    decode_sm103_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap kvh_map,
+                        const __grid_constant__ CUtensorMap q_map,
                         const __grid_constant__ CUtensorMap o_map, const __grid_constant__ CUtensorMap p_map,
                         const DecodeArgs p) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -232,38 +232,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0 && npages > 0) {
                 tma_prefetch_desc(&q_map);
                 tma_prefetch_desc(&kv_map);
-                // bf16 cache: the first K panels and the L2 prefetch go out before the preceding
-                // kernel (which may be writing q) has finished; the FP8 path's expanded rows are
-                // that kernel's output, so it waits first.
+                // bf16 cache: the first K panels go out before the preceding kernel (which may be
+                // writing q) has finished; the FP8 path's expanded rows are that kernel's output,
+                // so it waits first. No L2 prefetch: the SM's TMA unit is the narrow point of the
+                // K stream, and bulk prefetches issued through it delay the ring's own loads.
                 if constexpr (kFp8) griddep_wait();
                 bool q_issued = false;
                 int issued = 0;  // K panels issued
                 bool ok = true;
-                // L2 prefetch of whole pages kPrefetchGroups groups ahead of the ring, so that the
-                // ring's loads see L2 rather than DRAM latency.
-                const uint8_t* kv_rows = kFp8 ? reinterpret_cast<const uint8_t*>(p.fp8_rows) : p.cache;
-                const int pf_end = min(npages, kPPG * kPrefetchGroups);
-                for (int pg = 0; pg < pf_end; ++pg) {
-                    const int yr = page_row<kFp8>(p, g.b, g.page0 + pg);
-                    if (kFp8 || yr < p.num_blocks * kPage)
-                        bulk_prefetch_l2(kv_rows + (size_t)yr * kBf16RowBytes, kPage * kBf16RowBytes);
-                }
                 for (int gi = 0; gi < ngroups && ok; ++gi) {
                     int y[kPPG];
                     const int np = min(kPPG, npages - kPPG * gi);
                     for (int q = 0; q < np; ++q) y[q] = page_row<kFp8>(p, g.b, g.page0 + kPPG * gi + q);
-                    auto prefetch_ahead = [&]() {
-                        for (int q = 0; q < kPPG; ++q) {
-                            const int pg = kPPG * (gi + kPrefetchGroups) + q;
-                            if (pg >= npages) break;
-                            const int yr = page_row<kFp8>(p, g.b, g.page0 + pg);
-                            if (kFp8 || yr < p.num_blocks * kPage)
-                                bulk_prefetch_l2(kv_rows + (size_t)yr * kBf16RowBytes, kPage * kBf16RowBytes);
-                        }
-                    };
-                    // the first group's look-ahead waits until Q is on its way: every query
-                    // row's first MMA needs Q, and requests made earlier are served first
-                    if (gi > 0) prefetch_ahead();
                     for (int pn = 0; pn < 9; ++pn) {
                         const int m = 9 * gi + pn, slot = m % kSlots, k = m / kSlots;
                         if (!q_issued && m == 2) {  // Q: the preceding kernel's output
@@ -273,9 +253,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 tma_load_2d(sbase + q_panel_off(qn), &q_map, bar(B_QFULL), qn * 64, g.r * p.H);
                             tma_load_2d(sbase + OFF_QROPE, &q_map, bar(B_QFULL), 8 * 64, g.r * p.H);
                             q_issued = true;
-                            prefetch_ahead();
                         }
-                        // first use of slots 2 and 3: Q's panels have been moved out to TMEM
+                        // first use of slots 2-5: Q's panels have been moved out to TMEM
                         ok = k > 0      ? wait_bar(bar(B_SLOTEMPTY + slot), (k - 1) & 1, abort, ds)
                              : slot >= 2 ? wait_bar(bar(B_QREADY), 0, abort, ds)
                                          : true;
@@ -439,6 +418,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 l_run *= alpha;
                 lt_run *= alpha;
+                // does any row of this group move its max (then CTA 1 rescales O first); the
+                // barrier also keeps the next group's writes of mx behind this group's reads
+                const bool any = named_bar_or(kBarOr, 256, resc && gi > 0);
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const int page = pg0 + q;
@@ -467,30 +449,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                     }
                     if (page < npages && okS) {
-                        const int stg = page % kPBufs, ust = page / kPBufs;
-                        if (ust > 0 && !warp_wait<true>(bar(B_STAGEFREE + stg), (ust - 1) & 1, abort, ds)) continue;
-                        uint8_t* sbuf = smem + OFF_STAGE + stg * kPBufStride;
+                        // CTA 1's buffer for this page is free once the PV of the page kPBufs
+                        // earlier has completed (multicast commit)
+                        const int pb = page % kPBufs, up = page / kPBufs;
+                        if (up > 0 && !warp_wait<true>(bar(B_PEMPTY + pb), (up - 1) & 1, abort, ds)) continue;
+                        const uint32_t dst = pbuf_remote + pb * kPBufStride;
+                        const uint32_t fb = pfull_remote + 8u * pb;
 #pragma unroll
                         for (int c = 0; c < 8; ++c)
-                            *reinterpret_cast<uint4*>(sbuf + row * 128 + ((c ^ (row & 7)) << 4)) =
-                                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                        // every row's alpha rides with the group's first page
-                        if (half == 0 && q == 0) reinterpret_cast<float*>(sbuf + kPBytes)[row] = alpha;
-                        fence_proxy_async_cta();
-                    }
-                }
-                const bool any = named_bar_or(kBarOr, 256, resc && gi > 0);
-                if (tid == 64 && !*abort) {  // one thread ships the group's pages
-                    for (int q = 0; q < kPPG; ++q) {
-                        const int pg = kPPG * gi + q;
-                        if (pg >= npages) break;
-                        uint8_t* b = smem + OFF_STAGE + (pg % kPBufs) * kPBufStride;
-                        *reinterpret_cast<uint32_t*>(b + kPBytes + 512) = (q == 0 && any) ? 1u : 0u;
-                        fence_proxy_async_cta();
-                        const int pbi = pg % kPBufs, upb = pg / kPBufs;
-                        if (upb > 0 && !wait_bar<true>(bar(B_PEMPTY + pbi), (upb - 1) & 1, abort, ds)) break;
-                        bulk_copy_to_peer(pbuf_remote + pbi * kPBufStride, smem_addr(b), kPMsgBytes,
-                                          pfull_remote + 8u * pbi);
+                            st_async_v4(dst + row * 128 + ((c ^ (row & 7)) << 4),
+                                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]), fb);
+                        // every page carries the group's rescale factors; the group's first page
+                        // also carries the flag that tells CTA 1 to rescale O first
+                        st_async_b32(dst + kPBytes + 4 * row, __float_as_uint(alpha), fb);
+                        if (row == 0)
+                            st_async_b32(dst + kPBytes + 512, (half == 0 && q == 0 && any) ? 1u : 0u, fb);
                     }
                 }
             }
@@ -510,13 +483,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 named_bar(kBarHalf0, 128);
                 if (tid == 64) {
                     bar_arrive_remote(bar(B_STATS), 1);
-                    // nothing may still be on its way to this CTA when it exits
+                    // nothing may still be on its way to this CTA when it exits: CTA 1's last
+                    // multicast commits
                     for (int pg = (npages > kPBufs ? npages - kPBufs : 0); pg < npages; ++pg) {
                         volatile int dummy = 0;
                         wait_bar<true>(bar(B_PEMPTY + pg % kPBufs), (pg / kPBufs) & 1, *abort ? &dummy : abort, ds);
-                        dummy = 0;
-                        wait_bar<true>(bar(B_STAGEFREE + pg % kPBufs), (pg / kPBufs) & 1, *abort ? &dummy : abort,
-                                       ds);
                     }
                 }
             }
@@ -525,19 +496,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ============================== output CTA ==============================
         if (warp == 0) {
             if (lane == 0 && npages > 0) {
-                tma_prefetch_desc(&kv_map);
+                tma_prefetch_desc(&kvh_map);
                 if constexpr (kFp8) griddep_wait();  // expanded rows: the preceding kernel's output
+                // kVRows tokens x 512 dims per stage: stage hs holds rows
+                // [kVRows (hs % kVPerPage), + kVRows) of page hs / kVPerPage
                 int issued = 0;
-                for (int i = 0; i < npages; ++i) {
-                    const int st = i % kVStages, kv = i / kVStages;
-                    if (kv > 0 && !wait_bar(bar(B_VEMPTY + st), (kv - 1) & 1, abort, ds)) break;
-                    const uint32_t full = bar(B_VFULL + st);
-                    bar_arrive_expect_tx(full, kVStageBytes);
+                bool ok = true;
+                for (int i = 0; i < npages && ok; ++i) {
                     const int y = page_row<kFp8>(p, g.b, g.page0 + i);
-                    const uint32_t dst = sbase + OFF_V + st * kVStageBytes;
+                    for (int hf = 0; hf < kVPerPage; ++hf) {
+                        const int hs = kVPerPage * i + hf, st = hs % kVStages, kv = hs / kVStages;
+                        if (kv > 0 && !(ok = wait_bar(bar(B_VEMPTY + st), (kv - 1) & 1, abort, ds))) break;
+                        const uint32_t full = bar(B_VFULL + st);
+                        bar_arrive_expect_tx(full, kVStageBytes);
+                        const uint32_t dst = sbase + OFF_V + st * kVStageBytes;
 #pragma unroll
-                    for (int pn = 0; pn < 8; ++pn) tma_load_2d(dst + pn * kPageBox, &kv_map, full, pn * 64, y);
-                    issued = i + 1;
+                        for (int pn = 0; pn < 8; ++pn)
+                            tma_load_2d(dst + pn * kVBox, &kvh_map, full, pn * 64, y + kVRows * hf);
+                        issued = hs + 1;
+                    }
                 }
                 if (*abort) {
                     for (int i = (issued > kVStages ? issued - kVStages : 0); i < issued; ++i) {
@@ -547,34 +524,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
         } else if (warp == 1) {
-            // MMA thread: one wait per page (READY), then the page's 8 N=256 MMAs and commits
+            // MMA thread: per page one wait for P (PFULL) and the helpers (READY), then for each of
+            // its V stages the stage's wait and its MMAs of N = 256 (K steps x 2 column halves)
             if (lane == 0) {
-                int done = 0;
-                for (int i = 0; i < npages; ++i) {
-                    const int st = i % kVStages, pb = i % kPBufs;
-                    // V and P were written by the async proxy (TMA / bulk copy): the MMA thread
+                int done = 0;  // V stages whose MMAs were issued
+                bool ok = true;
+                for (int i = 0; i < npages && ok; ++i) {
+                    const int pb = i % kPBufs;
+                    // V and P were written by the async proxy (TMA / st.async): the MMA thread
                     // observes their barriers itself; READY adds the helpers' rescale / zeroing.
-                    if (!wait_bar(bar(B_VFULL + st), (i / kVStages) & 1, abort, ds)) break;
-                    if (!wait_bar(bar(B_PFULL + pb), (i / kPBufs) & 1, abort, ds)) break;
-                    if (!wait_bar(bar(B_READY + pb), (i / kPBufs) & 1, abort, ds)) break;
+                    if (!(ok = wait_bar(bar(B_PFULL + pb), (i / kPBufs) & 1, abort, ds))) break;
+                    if (!(ok = wait_bar(bar(B_READY + pb), (i / kPBufs) & 1, abort, ds))) break;
                     tc_fence_after();  // after a rescale by the helper warps' tcgen05.st
-                    const uint32_t vb = sbase + OFF_V + st * kVStageBytes;
                     const uint32_t pbuf = sbase + OFF_PB + pb * kPBufStride;
+                    for (int hf = 0; hf < kVPerPage && ok; ++hf) {
+                        const int hs = kVPerPage * i + hf, st = hs % kVStages;
+                        if (!(ok = wait_bar(bar(B_VFULL + st), (hs / kVStages) & 1, abort, ds))) break;
+                        const uint32_t vb = sbase + OFF_V + st * kVStageBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kPage / 16; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(pbuf + kk * 32, 16, 1024);
+                        for (int k = 0; k < kVRows / 16; ++k) {
+                            const int kk = (kVRows / 16) * hf + k;  // K step of the page
+                            const uint64_t ad = smem_desc_sw128(pbuf + kk * 32, 16, 1024);
 #pragma unroll
-                        for (int nh = 0; nh < 2; ++nh) {
-                            const uint64_t bd = smem_desc_sw128(vb + nh * 4 * kPageBox + kk * 2048, kPageBox, 1024);
-                            mma_ss(tmem + 256u * nh, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                            for (int nh = 0; nh < 2; ++nh) {
+                                const uint64_t bd = smem_desc_sw128(vb + nh * 4 * kVBox + k * 2048, kVBox, 1024);
+                                mma_ss(tmem + 256u * nh, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                            }
                         }
+                        mma_commit(bar(B_VEMPTY + st));
+                        done = hs + 1;
                     }
-                    mma_commit(bar(B_VEMPTY + st));
+                    if (!ok) break;
                     // P buffer pb is free again (CTA 0) and O holds page i (helper warps, CTA 1).
                     // One barrier per P buffer keeps every waiter within one phase of it: a
-                    // page's P only arrives after the PV of the page four earlier completed.
+                    // page's P only arrives after the PV of the page kPBufs earlier completed.
                     mma_commit_multicast(bar(B_PEMPTY + pb), (uint16_t)0x3);
-                    done = i + 1;
                 }
                 volatile int dummy = 0;  // drain the V-ring commits before teardown
                 for (int i = (done > kVStages ? done - kVStages : 0); i < done; ++i) {
@@ -591,13 +575,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int eset = warp >= 6 ? 1 : 0;
             int pages_ready = warp >= 6 ? npages : 0;
             for (int i = 0; i < npages && warp < 6; ++i) {
-                const int st = i % kVStages, kv = i / kVStages, pb = i % kPBufs, up = i / kPBufs;
+                const int pb = i % kPBufs, up = i / kPBufs;
                 if (!warp_wait(bar(B_PFULL + pb), up & 1, abort, ds)) break;
-                if (ctid == 0) {
-                    // the staging buffer in CTA 0 has been copied out; re-arm for the next message
-                    bar_arrive_remote(bar(B_STAGEFREE + pb), 0);
-                    bar_arrive_expect_tx(bar(B_PFULL + pb), kPMsgBytes);
-                }
+                if (ctid == 0) bar_arrive_expect_tx(bar(B_PFULL + pb), kPMsgBytes);  // re-arm for the next message
                 const uint8_t* pmsg = smem + OFF_PB + pb * kPBufStride;
                 const bool fix = i > 0 && *reinterpret_cast<const volatile uint32_t*>(pmsg + kPBytes + 512) != 0;
                 const int valid = valid_rows(g, i);
@@ -616,17 +596,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();
                 }
-                if (!warp_wait(bar(B_VFULL + st), kv & 1, abort, ds)) break;
-                if (valid < kPage) {  // zero V rows [valid, 64) of all 8 panels of the stage
-                    const uint32_t vb = OFF_V + st * kVStageBytes;
-                    const int chunks = (kPage - valid) * 8 * 8;
-                    for (int q = ctid; q < chunks; q += 128) {
-                        const int rr = valid + q / 64, pn = (q / 8) % 8, cc = q % 8;
-                        *reinterpret_cast<uint4*>(smem + vb + pn * kPageBox + rr * 128 + cc * 16) =
-                            make_uint4(0, 0, 0, 0);
+                bool vok = true;
+                for (int hf = 0; hf < kVPerPage && vok; ++hf) {
+                    const int hs = kVPerPage * i + hf, st = hs % kVStages;
+                    if (!(vok = warp_wait(bar(B_VFULL + st), (hs / kVStages) & 1, abort, ds))) break;
+                    // rows of this half past the last visible token: zero them in all 8 panels
+                    const int vh = min(kVRows, max(0, valid - kVRows * hf));
+                    if (vh < kVRows) {
+                        const uint32_t vb = OFF_V + st * kVStageBytes;
+                        const int chunks = (kVRows - vh) * 8 * 8;
+                        for (int q = ctid; q < chunks; q += 128) {
+                            const int rr = vh + q / 64, pn = (q / 8) % 8, cc = q % 8;
+                            *reinterpret_cast<uint4*>(smem + vb + pn * kVBox + rr * 128 + cc * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_cta();
                     }
-                    fence_proxy_async_cta();
                 }
+                if (!vok) break;
                 tc_fence_before();
                 bar_arrive(bar(B_READY + pb));
                 pages_ready = i + 1;
@@ -757,8 +744,9 @@ cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         g_attr_done[fp8][dev] = 1;
     }
-    CUtensorMap kv_map, q_map, o_map, p_map;
+    CUtensorMap kv_map, kvh_map, q_map, o_map, p_map;
     memset(&kv_map, 0, sizeof kv_map);
+    memset(&kvh_map, 0, sizeof kvh_map);
     memset(&q_map, 0, sizeof q_map);
     memset(&o_map, 0, sizeof o_map);
     memset(&p_map, 0, sizeof p_map);
@@ -793,12 +781,17 @@ cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s) {
         e = encode_tmap(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, fp8 ? (const void*)a.fp8_rows : a.cache, dims,
                         strides, box, true);
         if (e != cudaSuccess) return e;
+        // the same rows in boxes of kVRows tokens (CTA 1's V stages)
+        const uint32_t hbox[2] = {64, (uint32_t)kVRows};
+        e = encode_tmap(&kvh_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, fp8 ? (const void*)a.fp8_rows : a.cache, dims,
+                        strides, hbox, true);
+        if (e != cudaSuccess) return e;
         const uint64_t qdims[2] = {(uint64_t)kD, (uint64_t)a.rows * a.H};
         const uint32_t qbox[2] = {64, 128};
         e = encode_tmap(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, qdims, strides, qbox, true);
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(kernel, dim3((unsigned)(2 * units)), dim3(kThreads), kSmemBytes, s, kv_map, q_map, o_map,
+    return launch_pdl(kernel, dim3((unsigned)(2 * units)), dim3(kThreads), kSmemBytes, s, kv_map, kvh_map, q_map, o_map,
                       p_map, a);
 }
 

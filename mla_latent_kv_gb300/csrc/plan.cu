@@ -10,22 +10,24 @@
 // considered, so the unit count stays within rows + 2 pairs. A row that gets one unit writes its
 // final output directly; the units of a split row write fp32 partials that the merge combines.
 // The split points follow the same page-aligned rule as uniform splits (split_range).
+#include <algorithm>
+
 #include "internal.h"
 #include "sm103_ptx.cuh"
 
 namespace mla {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kMaxThreads = 1024;  // one CTA; the block size follows the row count (128..1024)
 constexpr int kCands = 13;
 constexpr int kSmemRows = 12288;  // rows whose page counts are kept in shared memory
 constexpr float kUnitCost = 6.f;  // fixed cost of one unit, in page-times
 
 __device__ __forceinline__ int pages_of(int n) { return (n + kPage - 1) / kPage; }
 
-// Inclusive block scan of one value per thread (1024 threads); returns the exclusive prefix.
+// Block scan of one value per thread; returns the exclusive prefix (and the block total).
 __device__ __forceinline__ long long block_exclusive_scan(long long v, long long* warp_tot, long long* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     long long x = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -35,7 +37,7 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
     if (lane == 31) warp_tot[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        long long w = warp_tot[lane];
+        long long w = lane < nwarps ? warp_tot[lane] : 0;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const long long y = __shfl_up_sync(0xffffffffu, w, off);
@@ -45,12 +47,12 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
     }
     __syncthreads();
     const long long before = (warp > 0 ? warp_tot[warp - 1] : 0) + x - v;
-    if (total) *total = warp_tot[31];
+    if (total) *total = warp_tot[nwarps - 1];
     __syncthreads();
     return before;
 }
 
-__global__ void __launch_bounds__(kThreads) plan_kernel(DecodeArgs p, int pairs) {
+__global__ void __launch_bounds__(kMaxThreads) plan_kernel(DecodeArgs p, int pairs) {
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();  // the schedule overwrites workspace an earlier kernel may still read
     __shared__ long long s_warp[32];
@@ -59,8 +61,8 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(DecodeArgs p, int pairs)
     __shared__ float s_cost[kCands];
     __shared__ int s_best;
     const int R = p.rows;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int per = (R + kThreads - 1) / kThreads;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const int per = (R + (int)blockDim.x - 1) / (int)blockDim.x;
     const int r0 = min(R, tid * per), r1 = min(R, r0 + per);
 
     // total and longest row, in pages
@@ -83,7 +85,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(DecodeArgs p, int pairs)
     __syncthreads();
     if (tid == 0) {
         int m = 0;
-        for (int w = 0; w < 32; ++w) m = max(m, s_mx[w]);
+        for (int w = 0; w < nwarps; ++w) m = max(m, s_mx[w]);
         const int longest = max(m, 1);
         const long long cmin = max(1LL, (total_pages + 2LL * pairs - 1) / (2LL * pairs));
         const float mult[kCands - 1] = {1.f, 1.25f, 1.5f, 2.f, 2.5f, 3.f, 4.f, 6.f, 8.f, 12.f, 16.f, 32.f};
@@ -99,8 +101,8 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(DecodeArgs p, int pairs)
     __syncthreads();
 
     // cost of each candidate (one warp each)
-    if (warp < kCands) {
-        const int c = s_cand[warp];
+    for (int k = warp; k < kCands; k += nwarps) {
+        const int c = s_cand[k];
         long long units = 0;
         int longest_unit = 0;
         for (int r = lane; r < R; r += 32) {
@@ -121,7 +123,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(DecodeArgs p, int pairs)
                 cost = fmaxf((float)longest_unit + kUnitCost,
                              waves * ((float)total_pages / (float)units + kUnitCost));
             }
-            s_cost[warp] = cost;
+            s_cost[k] = cost;
         }
     }
     __syncthreads();
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(DecodeArgs p, int pairs)
         }
         long long bucket_units = 0;
         long long ub = ubase_all + block_exclusive_scan(nu, s_warp, &bucket_units);
-        long long pb = bk == 0 ? block_exclusive_scan(nu, s_warp, nullptr) : 0;  // partial slots
+        long long pb = bk == 0 ? ub : 0;  // partial slots: bucket 0 comes first (ubase_all = 0)
         for (int r = r0; r < r1; ++r) {
             const int pg = pages(r);
             if (bucket_of(pg) != bk) continue;
@@ -182,7 +184,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(DecodeArgs p, int pairs)
 }  // namespace
 
 cudaError_t launch_plan(const DecodeArgs& a, int pairs, cudaStream_t s) {
-    return launch_pdl(plan_kernel, dim3(1), dim3(kThreads), 0, s, a, pairs);
+    // one row per thread where the batch allows it, so that few threads wait at each barrier
+    const int threads = (int)std::min<int64_t>(kMaxThreads, std::max<int64_t>(128, (a.rows + 31) / 32 * 32));
+    return launch_pdl(plan_kernel, dim3(1), dim3(threads), 0, s, a, pairs);
 }
 
 }  // namespace mla
