@@ -123,14 +123,11 @@ int mla_resolve_num_splits(int num_splits, int B, int Sq, int H, int max_seq_len
  * region 256-byte aligned. Host only. */
 size_t mla_decode_workspace_bytes(int B, int Sq, int H, int num_splits);
 
-/* Bytes of workspace mla_decode needs for a cache of format kv_dtype (valid for both formats;
- * for MLA_KV_BF16 it equals mla_decode_workspace_bytes). For the FP8 format it adds, after the
- * split-KV partials (each region 256-byte aligned), the first stage's expanded pages:
- * B * ceil(max_seq_len / 64) * 64 rows of 576 bf16 plus two fp32 scales per row. The 584-byte
- * FP8 row is not a multiple of 16 bytes, so TMA cannot tile it; mla_decode re-lays the pages a
- * batch reads out as exact bf16 values (e4m3 -> bf16 is lossless) and applies k_scale / v_scale
- * in fp32 inside the attention kernel. 0 for an unknown kv_dtype or a non-positive shape. Host
- * only. */
+/* Bytes of workspace mla_decode needs for a cache of format kv_dtype. It equals
+ * mla_decode_workspace_bytes for both formats: the FP8 cache's e4m3 values are widened to bf16
+ * (losslessly) in shared memory inside the attention kernel, and k_scale / v_scale are applied
+ * there in fp32, so the FP8 format needs no scratch of its own; max_seq_len does not change the
+ * result. 0 for an unknown kv_dtype or a non-positive shape. Host only. */
 size_t mla_decode_workspace_bytes_kv(mla_kv_dtype kv_dtype, int B, int Sq, int H, int num_splits,
                                      int max_seq_len);
 
@@ -181,9 +178,9 @@ mla_status mla_absorb_q(const void* q_nope, int64_t q_nope_stride_t, int64_t q_n
  *   o_latent    [B, Sq, H, 512] of o_dtype (fp32 recommended; bf16 rounds the result once)
  *   lse         fp32 [B, Sq, H], may be NULL
  *   dev_status  int32 device word or NULL; MLA_DEV_* bits are OR-ed into it, never cleared
- * Limits: 1 <= H <= 128, Sq >= 1, B >= 0 (B == 0 launches nothing), page size 64; FP8 cache:
- * ceil(max_seq_len / 64) <= 65535. FP8 precision: k_scale multiplies the fp32 score and v_scale
- * the fp32 softmax weight before its one rounding to bf16 for the PV product.
+ * Limits: 1 <= H <= 128, Sq >= 1, B >= 0 (B == 0 launches nothing), page size 64. FP8
+ * precision: k_scale multiplies the fp32 score and v_scale the fp32 softmax weight before its
+ * one rounding to bf16 for the PV product.
  */
 mla_status mla_decode(const void* q, const void* kv_cache, mla_kv_dtype kv_dtype, int64_t num_blocks,
                       const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
@@ -304,8 +301,8 @@ mla_status mla_prefill(const void* q, const void* kv_c, int64_t kv_c_stride_t, c
  * Same arguments, meaning and results as mla_decode, minus workspace / workspace_bytes. The
  * split-KV partials live in one file-scope device array of mla_decode_noalloc_max_workspace_bytes()
  * bytes (64 MiB), held on every device that uses it until the process exits; a call whose
- * mla_decode_workspace_bytes_kv exceeds that (most FP8-cache batches: the expanded pages live
- * in the same scratch) is refused with MLA_ERR_WORKSPACE_TOO_SMALL. The first call on a
+ * mla_decode_workspace_bytes_kv exceeds that (only split-KV partials count, for both cache
+ * formats) is refused with MLA_ERR_WORKSPACE_TOO_SMALL. The first call on a
  * device looks up the array's device address (once per device, with that device current); make
  * that first call before any stream capture. The address is reused while the device's context
  * stays the same; after a device reset the next call looks it up again (and is then again a

@@ -43,6 +43,7 @@
 
 #include <cstring>
 
+#include "decode_common.cuh"
 #include "internal.h"
 #include "sm103_ptx.cuh"
 
@@ -54,6 +55,7 @@ cudaError_t encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, c
 namespace {
 
 using namespace ptx;
+using namespace dec;
 
 constexpr int kThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (CTA 0) / 2-5 helpers, 2-9 epilogue (CTA 1)
 constexpr int kPPG = 4;              // pages per group
@@ -125,57 +127,6 @@ constexpr uint32_t kBarMax = 1, kBarOr = 2, kBarHalf0 = 3;  // named barriers of
 constexpr uint32_t kBarEpi = 4;                             // named barrier of CTA 1's helper warps
 constexpr int kEpiPanelBytes = 128 * 128;                   // 128 rows x 128 B output tile
 
-struct RowGeom {
-    int r, b, t, j0, j1, npages, page0;
-    int slot;  // partial-output slot, or -1: this unit writes the row's final output
-};
-
-__device__ __forceinline__ RowGeom row_geometry(const DecodeArgs& p, int unit, bool report) {
-    RowGeom g;
-    if (p.plan_units) {  // device-built schedule
-        const int4 u = p.plan_units[unit];
-        g.r = u.x;
-        g.j0 = u.y;
-        g.j1 = u.z;
-        g.slot = u.w;
-    } else {  // uniform splits: unit = row * S + split
-        const int S = p.num_splits;
-        g.r = unit / S;
-        split_range(visible_tokens(p, g.r, report), S, unit % S, &g.j0, &g.j1);
-        g.slot = S > 1 ? unit : -1;
-    }
-    int q_len;
-    row_request(p, g.r, &g.b, &g.t, &q_len);
-    g.npages = (g.j1 - g.j0 + kPage - 1) / kPage;
-    g.page0 = g.j0 / kPage;
-    return g;
-}
-
-// Physical first row of page `pg` of request b, or one past the cache (the TMA then fills
-// zeros) if the block-table entry is out of range. FP8 cache: the row in the expanded layout
-// (the first stage already resolved the block table and reported bad entries).
-template <bool kFp8>
-__device__ __forceinline__ int page_row(const DecodeArgs& p, int b, int pg) {
-    if constexpr (kFp8) return (b * p.fp8_mp + pg) * kPage;
-    int32_t blk = p.block_table[(size_t)b * p.max_blocks + pg];
-    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-        if (p.dev_status) atomicOr(p.dev_status, MLA_DEV_BAD_BLOCK_ID);
-        return (int)(p.num_blocks * kPage);
-    }
-    return blk * kPage;
-}
-
-template <bool kCluster = false>
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* ds) {
-    bool ok = wait_bar<kCluster>(bar, parity, abort, ds);
-    return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ int valid_rows(const RowGeom& g, int page) {
-    return page < g.npages ? min(kPage, g.j1 - (g.j0 + kPage * page)) : 0;
-}
-
-template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_sm103_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap kvh_map,
                         const __grid_constant__ CUtensorMap q_map,
@@ -232,22 +183,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0 && npages > 0) {
                 tma_prefetch_desc(&q_map);
                 tma_prefetch_desc(&kv_map);
-                // bf16 cache: the first K panels go out before the preceding kernel (which may be
-                // writing q) has finished; the FP8 path's expanded rows are that kernel's output,
-                // so it waits first. No L2 prefetch: the SM's TMA unit is the narrow point of the
-                // K stream, and bulk prefetches issued through it delay the ring's own loads.
-                if constexpr (kFp8) griddep_wait();
+                // The first K panels go out before the preceding kernel (which may be writing q)
+                // has finished: no kernel of this library writes the cache. No L2 prefetch: the
+                // SM's TMA unit is the narrow point of the K stream, and bulk prefetches issued
+                // through it delay the ring's own loads.
+                const int oob = (int)(p.num_blocks * kPage);  // one past the cache: TMA fills zeros
                 bool q_issued = false;
                 int issued = 0;  // K panels issued
                 bool ok = true;
                 for (int gi = 0; gi < ngroups && ok; ++gi) {
                     int y[kPPG];
                     const int np = min(kPPG, npages - kPPG * gi);
-                    for (int q = 0; q < np; ++q) y[q] = page_row<kFp8>(p, g.b, g.page0 + kPPG * gi + q);
+                    for (int q = 0; q < np; ++q) {
+                        const int blk = page_block(p, g.b, g.page0 + kPPG * gi + q);
+                        y[q] = blk < 0 ? oob : blk * kPage;
+                    }
                     for (int pn = 0; pn < 9; ++pn) {
                         const int m = 9 * gi + pn, slot = m % kSlots, k = m / kSlots;
                         if (!q_issued && m == 2) {  // Q: the preceding kernel's output
-                            if constexpr (!kFp8) griddep_wait();
+                            griddep_wait();
                             bar_arrive_expect_tx(bar(B_QFULL), 9 * kQPanelBytes);
                             for (int qn = 0; qn < 8; ++qn)
                                 tma_load_2d(sbase + q_panel_off(qn), &q_map, bar(B_QFULL), qn * 64, g.r * p.H);
@@ -377,32 +331,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 const int pg0 = kPPG * gi + 2 * half;  // first of this half's two pages
                 const int valid0 = valid_rows(g, pg0), valid1 = valid_rows(g, pg0 + 1);
-                // FP8 cache: lane i holds (k_scale, v_scale) of token i of each 32-token chunk;
-                // tokens past the last visible one keep 0 so that no stale scale reaches P.
-                float ksc[4] = {0.f, 0.f, 0.f, 0.f}, vsc[4] = {0.f, 0.f, 0.f, 0.f};
-                if constexpr (kFp8) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int v = c < 2 ? valid0 - 32 * c : valid1 - 32 * (c - 2);
-                        if (lane < v) {
-                            const size_t tok = ((size_t)g.b * p.fp8_mp + g.page0 + pg0 + (c >> 1)) * kPage +
-                                               32 * (c & 1) + lane;
-                            const float2 sc = reinterpret_cast<const float2*>(p.fp8_scales)[tok];
-                            ksc[c] = sc.x;
-                            vsc[c] = sc.y;
-                        }
-                    }
-                }
                 float lm = -CUDART_INF_F;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int v = c < 2 ? valid0 - 32 * c : valid1 - 32 * (c - 2);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        if constexpr (kFp8) {  // K = e4m3 * k_scale: the scale multiplies the score
-                            const float ks = __shfl_sync(0xffffffffu, ksc[c], j);
-                            s[c][j] = __float_as_uint(__uint_as_float(s[c][j]) * ks);
-                        }
                         if (j >= v) s[c][j] = __float_as_uint(-CUDART_INF_F);
                         lm = fmaxf(lm, __uint_as_float(s[c][j]));
                     }
@@ -431,22 +365,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const float a1 = fast_exp2(fmaf(__uint_as_float(s[2 * q][2 * c + 1]), sl2, -m_run));
                         const float b0 = fast_exp2(fmaf(__uint_as_float(s[2 * q + 1][2 * c]), sl2, -m_run));
                         const float b1 = fast_exp2(fmaf(__uint_as_float(s[2 * q + 1][2 * c + 1]), sl2, -m_run));
-                        if constexpr (kFp8) {
-                            // V = e4m3 * v_scale: the scale multiplies the weight before its one
-                            // rounding; O is normalised by the unscaled sum.
-                            pk[c] = pack_bf16x2(a0 * __shfl_sync(0xffffffffu, vsc[2 * q], 2 * c),
-                                                a1 * __shfl_sync(0xffffffffu, vsc[2 * q], 2 * c + 1));
-                            pk[16 + c] = pack_bf16x2(b0 * __shfl_sync(0xffffffffu, vsc[2 * q + 1], 2 * c),
-                                                     b1 * __shfl_sync(0xffffffffu, vsc[2 * q + 1], 2 * c + 1));
-                            lt_run += (a0 + a1) + (b0 + b1);
-                            l_run += (a0 + a1) + (b0 + b1);
-                        } else {
-                            pk[c] = pack_bf16x2(a0, a1);
-                            pk[16 + c] = pack_bf16x2(b0, b1);
-                            lt_run += (a0 + a1) + (b0 + b1);
-                            l_run += (bf16_lo_f(pk[c]) + bf16_hi_f(pk[c])) +
-                                     (bf16_lo_f(pk[16 + c]) + bf16_hi_f(pk[16 + c]));
-                        }
+                        pk[c] = pack_bf16x2(a0, a1);
+                        pk[16 + c] = pack_bf16x2(b0, b1);
+                        lt_run += (a0 + a1) + (b0 + b1);
+                        l_run += (bf16_lo_f(pk[c]) + bf16_hi_f(pk[c])) +
+                                 (bf16_lo_f(pk[16 + c]) + bf16_hi_f(pk[16 + c]));
                     }
                     if (page < npages && okS) {
                         // CTA 1's buffer for this page is free once the PV of the page kPBufs
@@ -497,13 +420,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (warp == 0) {
             if (lane == 0 && npages > 0) {
                 tma_prefetch_desc(&kvh_map);
-                if constexpr (kFp8) griddep_wait();  // expanded rows: the preceding kernel's output
                 // kVRows tokens x 512 dims per stage: stage hs holds rows
                 // [kVRows (hs % kVPerPage), + kVRows) of page hs / kVPerPage
                 int issued = 0;
                 bool ok = true;
                 for (int i = 0; i < npages && ok; ++i) {
-                    const int y = page_row<kFp8>(p, g.b, g.page0 + i);
+                    const int blk = page_block(p, g.b, g.page0 + i);
+                    const int y = blk < 0 ? (int)(p.num_blocks * kPage) : blk * kPage;  // TMA fills zeros
                     for (int hf = 0; hf < kVPerPage; ++hf) {
                         const int hs = kVPerPage * i + hf, st = hs % kVStages, kv = hs / kVStages;
                         if (kv > 0 && !(ok = wait_bar(bar(B_VEMPTY + st), (kv - 1) & 1, abort, ds))) break;
@@ -729,20 +652,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();
 }
 
-int g_attr_done[2][64] = {};
+int g_attr_done[64] = {};
 
 }  // namespace
 
 cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s) {
-    const bool fp8 = a.fp8_mp > 0;
-    auto* kernel = fp8 ? decode_sm103_kernel<true> : decode_sm103_kernel<false>;
+    auto* kernel = decode_sm103_kernel;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !g_attr_done[fp8][dev]) {
+    if (dev < 64 && !g_attr_done[dev]) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        g_attr_done[fp8][dev] = 1;
+        g_attr_done[dev] = 1;
     }
     CUtensorMap kv_map, kvh_map, q_map, o_map, p_map;
     memset(&kv_map, 0, sizeof kv_map);
@@ -773,17 +695,17 @@ cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     if (a.num_blocks > 0 && a.max_seq_len > 0) {
-        // bf16 rows of the cache itself, or of the FP8 cache's expanded pages
-        const uint64_t rows = fp8 ? (uint64_t)a.B * a.fp8_mp * kPage : (uint64_t)a.num_blocks * kPage;
+        // the cache's bf16 rows
+        const uint64_t rows = (uint64_t)a.num_blocks * kPage;
         const uint64_t dims[2] = {(uint64_t)kD, rows};
         const uint64_t strides[1] = {(uint64_t)kBf16RowBytes};
         const uint32_t box[2] = {64, 64};
-        e = encode_tmap(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, fp8 ? (const void*)a.fp8_rows : a.cache, dims,
+        e = encode_tmap(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.cache, dims,
                         strides, box, true);
         if (e != cudaSuccess) return e;
         // the same rows in boxes of kVRows tokens (CTA 1's V stages)
         const uint32_t hbox[2] = {64, (uint32_t)kVRows};
-        e = encode_tmap(&kvh_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, fp8 ? (const void*)a.fp8_rows : a.cache, dims,
+        e = encode_tmap(&kvh_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.cache, dims,
                         strides, hbox, true);
         if (e != cudaSuccess) return e;
         const uint64_t qdims[2] = {(uint64_t)kD, (uint64_t)a.rows * a.H};

@@ -38,10 +38,6 @@ struct DecodeArgs {
     int o_dtype;                // mla_dtype
     float* lse;                 // [B, Sq, H] or null
     int32_t* dev_status;        // or null
-    // FP8 cache only: pages expanded by the first stage into bf16 rows + per-token scales
-    uint16_t* fp8_rows;         // [B * fp8_mp * 64, 576] bf16 (exact e4m3 values)
-    float* fp8_scales;          // [B * fp8_mp * 64, 2] (k_scale, v_scale)
-    int fp8_mp;                 // pages per request in that layout: ceil(max_seq_len / 64)
     // Device-built schedule (num_splits == -2): unit u covers tokens [y, z) of query row x and
     // writes partial slot w (-1: the row's final output); row r's partials are slots
     // [rows[r].x, rows[r].x + rows[r].y) when rows[r].y > 1. Null in the uniform-split modes.
@@ -74,13 +70,13 @@ __device__ __forceinline__ void row_request(const DecodeArgs& p, int r, int* b, 
 }
 
 // Visible tokens of query row r: seq_len - (q_len - 1 - t), clamped at 0, with seq_len clamped
-// to what the block table (or the FP8 expansion) can hold; an out-of-range seq_len sets
+// to what the block table can hold; an out-of-range seq_len sets
 // MLA_DEV_SEQ_TOO_LONG when `report`.
 __device__ __forceinline__ int visible_tokens(const DecodeArgs& p, int r, bool report) {
     int b, t, q_len;
     row_request(p, r, &b, &t, &q_len);
     int seq = p.seq_lens[b];
-    const int cap = (p.fp8_mp > 0 && p.fp8_mp < p.max_blocks ? p.fp8_mp : p.max_blocks) * MLA_PAGE_SIZE;
+    const int cap = p.max_blocks * MLA_PAGE_SIZE;
     if (seq > cap || seq > p.max_seq_len || seq < 0) {
         if (report && p.dev_status) atomicOr(p.dev_status, MLA_DEV_SEQ_TOO_LONG);
         seq = seq < 0 ? 0 : (seq > cap ? cap : seq);
@@ -92,13 +88,13 @@ __device__ __forceinline__ int visible_tokens(const DecodeArgs& p, int r, bool r
 // Upper bound of planned units (num_splits == -2) for B * Sq query rows on `pairs` SM pairs.
 inline int64_t plan_max_units(int64_t rows, int pairs) { return rows + 2 * (int64_t)pairs; }
 
-// Workspace carve-up of a decode call: split-KV partials first, then (FP8 cache) the expanded
-// rows and their scales; every region starts on a 256-byte boundary.
+// Workspace carve-up of a decode call (the same for both cache formats): the device-built
+// schedule, then the split-KV partials; every region starts on a 256-byte boundary.
 struct WorkspaceLayout {
-    size_t plan, part_o, part_lse, fp8_rows, fp8_scales, total;
+    size_t plan, part_o, part_lse, total;
     int64_t partial_slots;  // rows of part_o / part_lse
 };
-// B requests (the FP8 expansion is per request) and `rows` query rows (split partials per row).
+// `rows` query rows (split partials per row); B, kv_dtype and max_seq_len do not change it.
 WorkspaceLayout workspace_layout(int kv_dtype, int B, int64_t rows, int H, int num_splits, int max_seq_len);
 
 // Token range [j0, j1) of split s of a row with n visible tokens: the row is cut into
@@ -136,8 +132,8 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 mla_status set_error(mla_status st, const char* fmt, ...);
 
 cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_fp8_sm103(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);
-cudaError_t launch_fp8_expand(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_plan(const DecodeArgs& a, int pairs, cudaStream_t s);
 cudaError_t launch_cache_write(const uint16_t* kv_c, int64_t st_c, const uint16_t* k_pe, int64_t st_pe,
                                const int64_t* slots, int T, uint8_t* cache, int kv_dtype, int64_t num_blocks,

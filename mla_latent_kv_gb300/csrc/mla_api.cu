@@ -69,13 +69,6 @@ WorkspaceLayout workspace_layout(int kv_dtype, int B, int64_t rows, int H, int n
         off = w.part_lse + up(units * sizeof(float));
         w.partial_slots = slots;
     }
-    if (kv_dtype == MLA_KV_FP8_E4M3_SCALED && max_seq_len > 0) {
-        const size_t rows = (size_t)B * ((max_seq_len + kPage - 1) / kPage) * kPage;
-        w.fp8_rows = off;
-        off += up(rows * kBf16RowBytes);
-        w.fp8_scales = off;
-        off += up(rows * 2 * sizeof(float));
-    }
     w.total = off;
     return w;
 }
@@ -222,8 +215,6 @@ mla_status decode_impl(const void* q, const void* kv_cache, mla_kv_dtype kv_dtyp
     if (rows > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "mla_decode: %lld query rows too many", (long long)rows);
     if (!aligned16(q) || (kv_cache && !aligned16(kv_cache)) || !aligned16(o_latent))
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: q, kv_cache and o_latent must be 16-byte aligned");
-    if (kv_dtype == MLA_KV_FP8_E4M3_SCALED && (max_seq_len + mla::kPage - 1) / mla::kPage > 65535)
-        return fail(MLA_ERR_UNSUPPORTED, "mla_decode: FP8 cache with max_seq_len=%d above 65535 pages", max_seq_len);
     if (num_blocks > (int64_t)(INT32_MAX / mla::kPage))
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: num_blocks=%lld too large (max %d)", (long long)num_blocks,
                     INT32_MAX / mla::kPage);
@@ -240,9 +231,8 @@ mla_status decode_impl(const void* q, const void* kv_cache, mla_kv_dtype kv_dtyp
     const size_t need = wl.total;
     if (need > 0 && (workspace == nullptr || workspace_bytes < need))
         return fail(MLA_ERR_WORKSPACE_TOO_SMALL,
-                    "mla_decode: workspace %zu bytes < %zu needed (%d splits%s)",
-                    workspace ? workspace_bytes : (size_t)0, need, S,
-                    kv_dtype == MLA_KV_FP8_E4M3_SCALED ? ", FP8 pages expanded" : "");
+                    "mla_decode: workspace %zu bytes < %zu needed (%d splits)",
+                    workspace ? workspace_bytes : (size_t)0, need, S);
     if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(MLA_ERR_UNSUPPORTED, "mla_decode: workspace must be 256-byte aligned");
 
@@ -273,27 +263,18 @@ mla_status decode_impl(const void* q, const void* kv_cache, mla_kv_dtype kv_dtyp
         a.plan_rows = (const int2*)(base + (256 + (size_t)max_units * sizeof(int4) + 255) / 256 * 256);
         a.plan_max_units = (int)max_units;
     }
-    const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3_SCALED && max_seq_len > 0;
-    if (fp8) {
-        a.fp8_rows = (uint16_t*)((char*)workspace + wl.fp8_rows);
-        a.fp8_scales = (float*)((char*)workspace + wl.fp8_scales);
-        a.fp8_mp = (max_seq_len + mla::kPage - 1) / mla::kPage;
-    }
+    const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3_SCALED;
     a.o_latent = o_latent;
     a.o_dtype = o_dtype;
     a.lse = lse;
     a.dev_status = dev_status;
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
-    if (fp8) {
-        e = mla::launch_fp8_expand(a, st);
-        if (e != cudaSuccess) return cuda_fail(e, "mla_decode FP8 expand launch");
-    }
     if (planned) {
         e = mla::launch_plan(a, pairs, st);
         if (e != cudaSuccess) return cuda_fail(e, "mla_decode schedule launch");
     }
-    e = mla::launch_decode_sm103(a, st);
+    e = fp8 ? mla::launch_decode_fp8_sm103(a, st) : mla::launch_decode_sm103(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
     if (planned || S > 1) {
         e = mla::launch_merge(a, st);

@@ -167,6 +167,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
         : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16) of contiguous global memory into this CTA's shared
+// memory; both addresses 16-byte aligned; completion counted (complete_tx) on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* gsrc, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // Prefetch `bytes` (a multiple of 16) of contiguous global memory into L2 (no shared memory,
 // no completion tracking).
 __device__ __forceinline__ void bulk_prefetch_l2(const void* gptr, uint32_t bytes) {
