@@ -91,6 +91,16 @@ const char* mla_last_error_detail(void);
  * NULL, MLA_ERR_CUDA if the launch fails. */
 mla_status mla_selftest_wait_timeout(int32_t* dev_status, int32_t* out, mla_stream_t stream);
 
+/* Self-test of the FP8 decode kernel's e4m3 -> bf16 widening ([vLLM-MLA, cache-shape section]:
+ * OCP FP8 E4M3 codes; the decode widens them to bf16 before the tensor-core MMAs): writes, for
+ * every code c = 0..255, the bf16 bits the kernel produces for it.
+ *   out   device uint16[256], caller-owned
+ * Every finite code's value is a bf16 value, and the kernel must produce it exactly (subnormal
+ * codes included); the two NaN codes 0x7F and 0xFF, which mla_cache_write never stores (it
+ * saturates), come out as +480 and -480. Asynchronous on `stream`. MLA_ERR_INVALID_ARG if out is
+ * NULL, MLA_ERR_CUDA if the launch fails. */
+mla_status mla_selftest_e4m3_widen(uint16_t* out, mla_stream_t stream);
+
 /* Bytes of one cached token row: 1152 (bf16) or 584 (FP8), -1 for an unknown format
  * ([vLLM-MLA, cache shape section]; [vLLM-MLA, numbers section]). Host only. */
 int64_t mla_kv_row_bytes(mla_kv_dtype kv_dtype);

@@ -49,6 +49,8 @@ def lib() -> ctypes.CDLL:
         l.mla_last_error_detail.argtypes = []
         l.mla_selftest_wait_timeout.restype = i32
         l.mla_selftest_wait_timeout.argtypes = [vp, vp, vp]
+        l.mla_selftest_e4m3_widen.restype = i32
+        l.mla_selftest_e4m3_widen.argtypes = [vp, vp]
         l.mla_kv_row_bytes.restype = i64
         l.mla_kv_row_bytes.argtypes = [i32]
         l.mla_default_num_splits.restype = i32
@@ -207,6 +209,12 @@ def selftest_wait_timeout(dev_status, out, stream=None):
     """Run the bounded-wait self-test: dev_status int32 [1] and out int32 [2] on the device; after a
     synchronise dev_status has MLA_DEV_WAIT_TIMEOUT set, out[0] is the wait in ms, out[1] is 0."""
     _check(lib().mla_selftest_wait_timeout(_p(dev_status), _p(out), _stream(stream)))
+
+
+def selftest_e4m3_widen(out, stream=None):
+    """Run the FP8 widening self-test: out uint16/int16 [256] on the device receives, after a
+    synchronise, the bf16 bits the FP8 decode kernel produces for e4m3 codes 0..255."""
+    _check(lib().mla_selftest_e4m3_widen(_p(out), _stream(stream)))
 
 
 def noalloc_max_workspace_bytes() -> int:

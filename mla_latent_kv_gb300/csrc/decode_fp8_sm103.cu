@@ -22,6 +22,9 @@
 //   - CTA 1 copies whole half pages (18,688 contiguous bytes) with one bulk copy each; eight
 //     converter warps widen the first 512 dims into the MN-major V tile and zero the rows past the
 //     last visible token.
+//   - Each softmax half stages its page of P (and the rescale factors) in its own shared memory
+//     and sends it with one bulk shared-to-shared copy: per-thread remote stores would queue in
+//     the same memory pipe as the converter warps' loads and stores.
 // All waits are bounded; on a timeout the kernel winds down and reports MLA_DEV_WAIT_TIMEOUT.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -51,7 +54,7 @@ constexpr int kPairBytes = 2 * kFp8RowBytes;      // 1168: one row pair of the c
 constexpr int kBoxW = 208;                        // raw box width (bytes): 192 dims + 16
 constexpr int kBoxBytes = 32 * kBoxW;             // one box: 32 row pairs of one page (6,656 B)
 constexpr int kRawSlotBytes = 2 * 2 * kBoxBytes;  // one triple of a group: [page][parity] boxes
-constexpr int kRawSlots = 4;
+constexpr int kRawSlots = 3;
 constexpr int kKPanelBytes = 128 * 128;           // one 64-dim panel of a group's 128 rows, bf16
 constexpr int kKSlotBytes = 3 * kKPanelBytes;     // one triple (48 KB)
 constexpr int kKSlots = 2;
@@ -64,36 +67,42 @@ constexpr int kVStageBytes = 8 * kVBox;           // 32 KB
 constexpr int kVStages = 2;
 constexpr int kPBufs = 5;                         // CTA 1 P buffers (one page each)
 constexpr int kPBytes = 128 * 128;                // P page: 128 heads x 64 tokens bf16
-constexpr int kPMsgBytes = kPBytes + 512 + 4;     // P + alpha[128] + flag word, stored by st.async
+// P + alpha[128] + flag word, padded to a multiple of 16 bytes: one bulk copy per page
+constexpr int kPMsgBytes = (kPBytes + 512 + 4 + 15) / 16 * 16;
 constexpr int kPBufStride = 17 * 1024;
-constexpr int kCtrlBytes = 8192;
+constexpr int kCtrlBytes = 3584;                             // barriers and small arrays, last
 // CTA 0 layout
-constexpr int OFF_QROPE = kCtrlBytes;                        // 16 KB
+constexpr int OFF_QROPE = 0;                                 // 16 KB
 constexpr int OFF_KRING = OFF_QROPE + kQPanelBytes;          // 2 x 48 KB
-constexpr int OFF_RAW = OFF_KRING + kKSlots * kKSlotBytes;   // 4 x 26 KB
-constexpr int kSmem0 = OFF_RAW + kRawSlots * kRawSlotBytes;
-// CTA 1 layout
-constexpr int OFF_V = kCtrlBytes;                            // 2 x 32 KB
+constexpr int OFF_RAW = OFF_KRING + kKSlots * kKSlotBytes;   // 3 x 26 KB
+constexpr int OFF_STAGE = OFF_RAW + kRawSlots * kRawSlotBytes;  // 2 x P message (one per half)
+constexpr int OFF_CTRL = OFF_STAGE + 2 * kPMsgBytes;
+constexpr int kSmem0 = OFF_CTRL + kCtrlBytes;
+// CTA 1 layout (the control block sits at the same offset in both CTAs)
+constexpr int OFF_V = 0;                                     // 2 x 32 KB
 constexpr int OFF_VRAW = OFF_V + kVStages * kVStageBytes;    // 3 x 18,688 B
 constexpr int OFF_PB = (OFF_VRAW + kVRawSlots * kHalfPageBytes + 1023) / 1024 * 1024;
 constexpr int kSmem1 = OFF_PB + kPBufs * kPBufStride;
-constexpr int kSmemBytes = kSmem0 > kSmem1 ? kSmem0 : kSmem1;
+static_assert(kSmem1 <= OFF_CTRL, "CTA 1's buffers end below the control block");
+constexpr int kSmemBytes = kSmem0;
 static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
 static_assert(kPMsgBytes <= kPBufStride, "P message");
 static_assert(kPairBytes % 16 == 0 && kBoxW % 16 == 0 && (576 % 16) == 0 && (192 % 16) == 0,
               "TMA: row-pair stride, box width and every box's x offset are multiples of 16 bytes");
 static_assert(kHalfPageBytes % 16 == 0 && OFF_VRAW % 16 == 0, "bulk copies of half pages");
+static_assert(OFF_STAGE % 1024 == 0 && kPMsgBytes % 16 == 0 && kPMsgBytes <= kPBufStride,
+              "P staging: bulk copies of whole messages; Q panels 6-7 land there first");
 static_assert(OFF_KRING % 1024 == 0 && OFF_RAW % 1024 == 0 && kRawSlotBytes % 1024 == 0 && OFF_PB % 1024 == 0 &&
                   kPBufStride % 1024 == 0 && kVBox % 1024 == 0 && OFF_V % 1024 == 0,
               "128-byte swizzled tiles need 1024-byte alignment");
 static_assert(kBoxBytes % 128 == 0, "TMA boxes start on 128-byte boundaries");
-// Q's latent panels land in the K ring (panels 0-5) and raw slots 2-3 (panels 6-7) until the
-// softmax warps move them to TMEM.
-static_assert(6 * kQPanelBytes == kKSlots * kKSlotBytes && 2 * kQPanelBytes <= 2 * kRawSlotBytes, "Q panel homes");
+// Q's latent panels land in the K ring (panels 0-5) and the P staging area (panels 6-7) until
+// the softmax warps move them to TMEM.
+static_assert(6 * kQPanelBytes == kKSlots * kKSlotBytes && 2 * kQPanelBytes <= 2 * kPMsgBytes, "Q panel homes");
 // the epilogue stages its output tiles over the V ring, the raw ring and the P buffers
 static_assert(OFF_V + 8 * 128 * 128 <= kSmem1, "epilogue tiles");
 __device__ __forceinline__ uint32_t q_panel_off(int pn) {
-    return pn < 6 ? OFF_KRING + pn * kQPanelBytes : OFF_RAW + 2 * kRawSlotBytes + (pn - 6) * kQPanelBytes;
+    return pn < 6 ? OFF_KRING + pn * kQPanelBytes : OFF_STAGE + (pn - 6) * kQPanelBytes;
 }
 
 // Barrier slots (8 bytes each); one layout for both CTAs so that a multicast commit from CTA 1
@@ -117,18 +126,20 @@ enum : int {
     B_PFULL = B_VEMPTY + kVStages,       // [kPBufs] CTA1: P message landed (st.async bytes from CTA0)
     B_READY = B_PFULL + kPBufs,          // [kPBufs] CTA1: O rescaled for the page (128 helper threads)
     B_STATS = B_READY + kPBufs,          // CTA1: final row statistics written by CTA0
-    B_COUNT
+    B_STAGEFREE,                         // [2] CTA0: a half's last P message has landed in CTA 1
+    B_COUNT = B_STAGEFREE + 2
 };
-static_assert(8 * B_COUNT <= 512, "barrier slots");
-constexpr int OFF_TMEM = 512;
-constexpr int OFF_ABORT = 516;
-constexpr int OFF_VRAW_OK = 528;   // CTA1: int [kVRawSlots] raw half page copied (0: bad block)
-constexpr int OFF_MX = 1024;       // CTA0: f32 [2][128] exchange between the two warp halves
-constexpr int OFF_KSC = 2048;      // CTA0: f32 [2 groups][128 tokens] k_scale
-constexpr int OFF_VSC = 3072;      // CTA0: f32 [2 groups][128 tokens] v_scale
-constexpr int OFF_STAT_M = 2048;   // CTA1: f32 [128] final running max (log2 units)
-constexpr int OFF_STAT_L = 2560;   // CTA1: f32 [128] row sum of P (normalises O)
-constexpr int OFF_STAT_LT = 3072;  // CTA1: f32 [128] the same sum (gives the LSE)
+static_assert(8 * B_COUNT <= 384, "barrier slots");
+constexpr int OFF_TMEM = OFF_CTRL + 384;
+constexpr int OFF_ABORT = OFF_CTRL + 388;
+constexpr int OFF_VRAW_OK = OFF_CTRL + 392;   // CTA1: int [kVRawSlots] raw half page copied (0: bad block)
+constexpr int OFF_MX = OFF_CTRL + 512;        // CTA0: f32 [2][128] exchange between the two warp halves
+constexpr int OFF_KSC = OFF_CTRL + 1536;      // CTA0: f32 [2 groups][128 tokens] k_scale
+constexpr int OFF_VSC = OFF_CTRL + 2560;      // CTA0: f32 [2 groups][128 tokens] v_scale
+constexpr int OFF_STAT_M = OFF_CTRL + 512;    // CTA1: f32 [128] final running max (log2 units)
+constexpr int OFF_STAT_L = OFF_CTRL + 1024;   // CTA1: f32 [128] row sum of P (normalises O)
+constexpr int OFF_STAT_LT = OFF_CTRL + 1536;  // CTA1: f32 [128] the same sum (gives the LSE)
+static_assert(OFF_VSC + 1024 <= OFF_CTRL + kCtrlBytes && OFF_VRAW_OK + 4 * kVRawSlots <= OFF_MX, "control block");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 256;  // CTA0: S buffer sb in columns [256 + 128 sb, + 128)
@@ -136,13 +147,16 @@ constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kBarMax = 1, kBarOr = 2, kBarHalf0 = 3;  // named barriers of the softmax warps
+constexpr uint32_t kBarStage0 = 5;                          // + half: one half's P staging
 constexpr uint32_t kBarEpi = 4;                             // named barrier of CTA 1's epilogue warps
 constexpr int kEpiPanelBytes = 128 * 128;
 
 // Eight e4m3 codes -> eight bf16 (exact), as one 16-byte chunk of a bf16 row.
 __device__ __forceinline__ uint4 widen8(uint2 v) {
-    return make_uint4(e4m3x2_to_bf16x2(v.x & 0xffffu), e4m3x2_to_bf16x2(v.x >> 16), e4m3x2_to_bf16x2(v.y & 0xffffu),
-                      e4m3x2_to_bf16x2(v.y >> 16));
+    uint4 o;
+    e4m3x4_to_bf16x4(v.x, o.x, o.y);
+    e4m3x4_to_bf16x4(v.y, o.z, o.w);
+    return o;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -167,7 +181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const RowGeom g = row_geometry(p, unit, tid == 0 && rank == 0);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
     int32_t* ds = p.dev_status;
-    auto bar = [&](int i) -> uint32_t { return sbase + 8u * (uint32_t)i; };
+    auto bar = [&](int i) -> uint32_t { return sbase + OFF_CTRL + 8u * (uint32_t)i; };
     const int npages = g.npages;
     const int ngroups = (npages + kPPG - 1) / kPPG;
 
@@ -228,11 +242,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             tma_load_2d(sbase + OFF_QROPE, &q_map, bar(B_QFULL), 8 * 64, g.r * p.H);
                             q_issued = true;
                         }
-                        // first use of slots 2 and 3: Q's panels 6 and 7 have been moved to TMEM
-                        ok = k > 0      ? wait_bar(bar(B_RAWEMPTY + slot), (k - 1) & 1, abort, ds)
-                             : slot >= 2 ? wait_bar(bar(B_QREADY), 0, abort, ds)
-                                         : true;
-                        if (!ok) break;
+                        if (k > 0 && !(ok = wait_bar(bar(B_RAWEMPTY + slot), (k - 1) & 1, abort, ds))) break;
                         const uint32_t full = bar(B_RAWFULL + slot);
                         const uint32_t dst = sbase + OFF_RAW + slot * kRawSlotBytes;
                         bar_arrive_expect_tx(full, np * 2 * kBoxBytes);
@@ -419,21 +429,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 bar_arrive(bar(B_SCEMPTY + sb));
-                if (page < npages && okS) {
+                // P goes to CTA 1 as one bulk copy per page from this half's staging buffer (the
+                // copy engine moves it; per-thread remote stores would queue behind the converter
+                // warps' shared-memory traffic). The buffer is rewritten only after the previous
+                // group's message from this half has landed (CTA 1's helpers signal it).
+                const int htid = tid - 64 - 128 * half;  // 0..127 within the half
+                uint8_t* stage = smem + OFF_STAGE + half * kPMsgBytes;
+                if (gi > 0) warp_wait<true>(bar(B_STAGEFREE + half), (gi - 1) & 1, abort, ds);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(stage + row * 128 + ((c ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                // every page carries the group's rescale factors; the group's first page also
+                // carries the flag that tells CTA 1 to rescale O first
+                reinterpret_cast<float*>(stage + kPBytes)[row] = alpha;
+                if (row == 0) *reinterpret_cast<uint32_t*>(stage + kPBytes + 512) = (half == 0 && any) ? 1u : 0u;
+                fence_proxy_async_cta();  // generic writes before the copy engine reads them
+                named_bar(kBarStage0 + half, 128);
+                if (htid == 0 && page < npages && okS) {
                     // CTA 1's buffer for this page is free once the PV of the page kPBufs earlier
                     // has completed (multicast commit)
                     const int pb = page % kPBufs, up = page / kPBufs;
-                    if (up > 0 && !warp_wait<true>(bar(B_PEMPTY + pb), (up - 1) & 1, abort, ds)) continue;
-                    const uint32_t dst = pbuf_remote + pb * kPBufStride;
-                    const uint32_t fb = pfull_remote + 8u * pb;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        st_async_v4(dst + row * 128 + ((c ^ (row & 7)) << 4),
-                                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]), fb);
-                    // every page carries the group's rescale factors; the group's first page also
-                    // carries the flag that tells CTA 1 to rescale O first
-                    st_async_b32(dst + kPBytes + 4 * row, __float_as_uint(alpha), fb);
-                    if (row == 0) st_async_b32(dst + kPBytes + 512, (half == 0 && any) ? 1u : 0u, fb);
+                    if (up == 0 || wait_bar<true>(bar(B_PEMPTY + pb), (up - 1) & 1, abort, ds)) {
+                        bulk_copy_to_peer(pbuf_remote + pb * kPBufStride, sbase + OFF_STAGE + half * kPMsgBytes,
+                                          kPMsgBytes, pfull_remote + 8u * pb);
+                    }
                 }
             }
             // combine the two halves' sums, ship the final statistics
@@ -478,19 +498,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         ok = m >= kKSlots ? warp_wait(bar(B_KEMPTY + ks), ((m / kKSlots) - 1) & 1, abort, ds)
                                           : warp_wait(bar(B_QREADY), 0, abort, ds);
                         if (!ok) break;
-                        const uint8_t* raw = smem + OFF_RAW + rs * kRawSlotBytes;
-                        uint8_t* kb = smem + OFF_KRING + ks * kKSlotBytes;
-#pragma unroll 4
-                        for (int k = 0; k < 24; ++k) {
-                            const int item = ctid + 128 * k;
-                            const int c = item & 7, R = (item >> 3) & 127, i = item >> 10;
-                            const int q = R >> 6, r = R & 63, e = r & 1, j = r >> 1;
-                            if (q < np) {
+                        const uint32_t raw = sbase + OFF_RAW + rs * kRawSlotBytes;
+                        const uint32_t kb = sbase + OFF_KRING + ks * kKSlotBytes;
+                        // eight loads, then eight widen-and-store: the compiler cannot move a load
+                        // above an earlier store to shared memory, so batching keeps loads in flight
+#pragma unroll 1
+                        for (int k0 = 0; k0 < 24; k0 += 8) {
+                            uint2 v[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                const int item = ctid + 128 * (k0 + u);
+                                const int c = item & 7, R = (item >> 3) & 127, i = item >> 10;
+                                const int q = R >> 6, r = R & 63, e = r & 1, j = r >> 1;
                                 // even rows start at the box's first byte, odd rows 8 bytes in
-                                const uint2 v = *reinterpret_cast<const uint2*>(
-                                    raw + (2 * q + e) * kBoxBytes + j * kBoxW + 8 * e + 64 * i + 8 * c);
-                                *reinterpret_cast<uint4*>(kb + i * kKPanelBytes + R * 128 + ((c ^ (R & 7)) << 4)) =
-                                    widen8(v);
+                                v[u] = q < np ? lds_u2(raw + (2 * q + e) * kBoxBytes + j * kBoxW + 8 * e + 64 * i + 8 * c)
+                                              : make_uint2(0u, 0u);
+                            }
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                const int item = ctid + 128 * (k0 + u);
+                                const int c = item & 7, R = (item >> 3) & 127, i = item >> 10;
+                                if ((R >> 6) < np) sts_u4(kb + i * kKPanelBytes + R * 128 + ((c ^ (R & 7)) << 4), widen8(v[u]));
                             }
                         }
                         if (t == 2) {
@@ -502,9 +530,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 break;
                             const int q = ctid >> 6, r = ctid & 63, e = r & 1, j = r >> 1;
                             float2 sc = make_float2(0.f, 0.f);
-                            if (q < np && r < valid_rows(g, kPPG * gi + q))
-                                sc = *reinterpret_cast<const float2*>(raw + (2 * q + e) * kBoxBytes + j * kBoxW + 8 * e +
-                                                                      192);
+                            if (q < np && r < valid_rows(g, kPPG * gi + q)) {
+                                const uint2 w = lds_u2(raw + (2 * q + e) * kBoxBytes + j * kBoxW + 8 * e + 192);
+                                sc = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+                            }
                             reinterpret_cast<float*>(smem + OFF_KSC)[128 * sb + ctid] = sc.x;
                             reinterpret_cast<float*>(smem + OFF_VSC)[128 * sb + ctid] = sc.y;
                             bar_arrive(bar(B_SCFULL + sb));
@@ -601,7 +630,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < npages; ++i) {
                     const int pb = i % kPBufs, up = i / kPBufs;
                     if (!warp_wait(bar(B_PFULL + pb), up & 1, abort, ds)) break;
-                    if (ctid == 0) bar_arrive_expect_tx(bar(B_PFULL + pb), kPMsgBytes);  // the next message
+                    if (ctid == 0) {
+                        bar_arrive_expect_tx(bar(B_PFULL + pb), kPMsgBytes);  // the next message
+                        bar_arrive_remote(bar(B_STAGEFREE + (i & 1)), 0);   // CTA 0 may restage
+                    }
                     const uint8_t* pmsg = smem + OFF_PB + pb * kPBufStride;
                     const bool fix = i > 0 && *reinterpret_cast<const volatile uint32_t*>(pmsg + kPBytes + 512) != 0;
                     if (fix) {  // O must hold every earlier PV product before it is rescaled
@@ -640,16 +672,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             !(ok = warp_wait(bar(B_VEMPTY + st), ((hs / kVStages) - 1) & 1, abort, ds)))
                             break;
                         const bool copied = *reinterpret_cast<const volatile int*>(raw_ok + rs) != 0;
-                        const uint8_t* raw = smem + OFF_VRAW + rs * kHalfPageBytes;
-                        uint8_t* vb = smem + OFF_V + st * kVStageBytes;
-#pragma unroll 4
+                        const uint32_t raw = sbase + OFF_VRAW + rs * kHalfPageBytes;
+                        const uint32_t vb = sbase + OFF_V + st * kVStageBytes;
+                        // all eight loads first (see the K converters)
+                        uint2 v[8];
+#pragma unroll
                         for (int k = 0; k < 8; ++k) {
                             const int item = ctid + 256 * k;
                             const int c = item & 7, pn = (item >> 3) & 7, r = item >> 6;
-                            uint4 out = make_uint4(0, 0, 0, 0);
-                            if (copied && kVRows * hf + r < valid)
-                                out = widen8(*reinterpret_cast<const uint2*>(raw + r * kFp8RowBytes + 64 * pn + 8 * c));
-                            *reinterpret_cast<uint4*>(vb + pn * kVBox + r * 128 + ((c ^ (r & 7)) << 4)) = out;
+                            v[k] = copied && kVRows * hf + r < valid ? lds_u2(raw + r * kFp8RowBytes + 64 * pn + 8 * c)
+                                                                     : make_uint2(0u, 0u);
+                        }
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int item = ctid + 256 * k;
+                            const int c = item & 7, pn = (item >> 3) & 7, r = item >> 6;
+                            sts_u4(vb + pn * kVBox + r * 128 + ((c ^ (r & 7)) << 4), widen8(v[k]));
                         }
                         fence_proxy_async_cta();  // generic-proxy writes before the MMAs read them
                         bar_arrive(bar(B_VFULL + st));

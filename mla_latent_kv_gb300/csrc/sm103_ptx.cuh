@@ -98,25 +98,53 @@ __device__ __forceinline__ bool bar_try_wait_cluster(uint32_t bar, uint32_t pari
     return ok != 0;
 }
 
+// try_wait that suspends the thread until the phase completes or `ns` nanoseconds pass: a
+// waiting warp then takes no issue slots from the warps that do the work on its SM sub-partition.
+__device__ __forceinline__ bool bar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool bar_try_wait_cluster_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kWaitSuspendNs = 20000;  // one suspended probe; the time limit is checked after each
+
 // The polling loop of wait_bar(), kept out of line: inlined at every wait, the loop costs a
 // waiting thread about 100 cycles even when the phase has already completed, which a thread that
-// issues MMAs between waits pays in tensor-pipe time.
+// issues MMAs between waits pays in tensor-pipe time. Each probe suspends the thread (until the
+// phase completes, or for at most kWaitSuspendNs) instead of spinning.
 template <bool kClusterScope>
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* dev_status) {
     uint64_t t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        bool done = kClusterScope ? bar_try_wait_cluster(bar, parity) : bar_try_wait(bar, parity);
+    for (;;) {
+        bool done = kClusterScope ? bar_try_wait_cluster_sleep(bar, parity, kWaitSuspendNs)
+                                  : bar_try_wait_sleep(bar, parity, kWaitSuspendNs);
         if (done) return true;
-        if ((it & 63u) == 63u) {
-            if (*abort) return false;
-            uint64_t now = global_timer_ns();
-            if (t0 == 0) {
-                t0 = now;
-            } else if (now - t0 > kWaitTimeoutNs) {
-                *abort = 1;
-                if (dev_status) atomicOr(dev_status, MLA_DEV_WAIT_TIMEOUT);
-                return false;
-            }
+        if (*abort) return false;
+        const uint64_t now = global_timer_ns();
+        if (t0 == 0) {
+            t0 = now;
+        } else if (now - t0 > kWaitTimeoutNs) {
+            *abort = 1;
+            if (dev_status) atomicOr(dev_status, MLA_DEV_WAIT_TIMEOUT);
+            return false;
         }
     }
 }
@@ -213,6 +241,24 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, uint32_t 
     asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      remote_dst),
                  "r"(local_src), "r"(bytes), "r"(remote_bar)
+                 : "memory");
+}
+
+// Shared-memory accesses by 32-bit shared-window address, so that they are always compiled as
+// shared-space loads and stores (never as generic accesses that resolve the window at run time).
+__device__ __forceinline__ uint2 lds_u2(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts_u4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
 
@@ -381,6 +427,23 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_bytes) {
         : "=f"(lo), "=f"(hi)
         : "r"(h2));
     return pack_bf16x2(lo, hi);
+}
+
+// Four OCP E4M3 values (bytes of w, lowest first) -> four bf16 in two words (lo: codes 0-1, hi:
+// codes 2-3), with integer and bf16 arithmetic only (no conversion instructions, whose throughput
+// is a quarter of the arithmetic pipes'). A code's magnitude bits eeee.mmm placed at bits 4-10 of a
+// bf16 are that bf16's exponent and leading mantissa bits, so the bf16 reads as the code's value
+// times 2^-120 -- for e = 0 as a bf16 subnormal, which is exactly the e4m3 subnormal m/8 * 2^-6
+// times 2^-120. One exact bf16 multiply by 2^120 restores the value. The two e4m3 NaN codes (never
+// written by the cache writer, which saturates) come out as +-480.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    constexpr uint32_t kTwoPow120 = 0x7B807B80u;  // bf16x2 (2^120, 2^120)
+    const uint32_t a = __byte_perm(w, 0u, 0x1404);  // [0, code0, 0, code1]
+    const uint32_t b = __byte_perm(w, 0u, 0x3424);  // [0, code2, 0, code3]
+    const uint32_t ab = ((a >> 4) & 0x07F007F0u) | (a & 0x80008000u);
+    const uint32_t bb = ((b >> 4) & 0x07F007F0u) | (b & 0x80008000u);
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(ab), "r"(kTwoPow120));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(bb), "r"(kTwoPow120));
 }
 
 }  // namespace ptx

@@ -119,6 +119,25 @@ def test_fp8_causal_two_rows_and_heads():
     compare_decode(o, lse, o_ref, lse_ref, fp8=True)
 
 
+def test_fp8_widening_is_exact_for_every_code():
+    """The FP8 decode kernel widens e4m3 codes with integer and bf16 arithmetic (no conversion
+    instructions). Every finite code, subnormals included, must come out as its exact value (the
+    oracle's e4m3 decode); the two NaN codes, which the cache writer never stores, read +-480."""
+    import torch
+    import mla_latent_kv_gb300 as mla
+    out = torch.zeros(256, dtype=torch.int16, device="cuda")
+    mla.selftest_e4m3_widen(out)
+    torch.cuda.synchronize()
+    got = oracle.widen_bf16(out.cpu().numpy().view(np.uint16))
+    for code in range(256):
+        want = {0x7F: 480.0, 0xFF: -480.0}.get(code, None)
+        if want is None:
+            want = oracle.e4m3_value(code)
+        assert got[code] == want, (code, got[code], want)
+    # the sign of zero survives too
+    assert np.signbit(got[0x80]) and not np.signbit(got[0x00])
+
+
 def test_fp8_bad_block_id_sets_device_status():
     c = _fp8_case(2, 1, 16, [100, 100], seed=28)
     bt = c["block_table"].copy()
