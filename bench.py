@@ -68,26 +68,30 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-DECODE_SOURCES = ("decode_sm103.cu", "sm103_ptx.cuh", "internal.h")  # what the decode kernel compiles from
+# what each decode kernel compiles from (bf16 cache, FP8 cache)
+DECODE_SOURCES = {
+    "decode_sm103.cu": ("decode_sm103.cu", "decode_common.cuh", "sm103_ptx.cuh", "internal.h"),
+    "decode_fp8_sm103.cu": ("decode_fp8_sm103.cu", "decode_common.cuh", "sm103_ptx.cuh", "internal.h"),
+}
 
 
-def decode_kernel_sha256():
-    """sha256 over the decode kernel's source files, in DECODE_SOURCES order."""
+def decode_kernel_sha256(kernel="decode_sm103.cu"):
+    """sha256 over one decode kernel's source files, in DECODE_SOURCES order."""
     h = hashlib.sha256()
-    for name in DECODE_SOURCES:
+    for name in DECODE_SOURCES[kernel]:
         with open(os.path.join(ROOT, "mla_latent_kv_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def measured_traffic(workload):
+def measured_traffic(workload, kernel="decode_sm103.cu"):
     """DRAM bytes per decode launch from the committed ncu capture (profiles/traffic.json), or
     None when that capture was of another workload (name and o_latent dtype, e.g. "dsv3/o_bf16")
     or of a different decode kernel source."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f)["decode_sm103.cu"]
-        h = decode_kernel_sha256()
+            rec = json.load(f)[kernel]
+        h = decode_kernel_sha256(kernel)
     except (OSError, KeyError, ValueError):
         return None
     w = rec.get("workloads", {}).get(workload)
@@ -409,6 +413,7 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     byts, flops, kv_bytes = algorithmic(c, o_bytes=2 if args.o_dtype == "bf16" else 4)
     traffic_key = f"{args.workload}/o_{args.o_dtype}"
+    traffic_kernel = "decode_fp8_sm103.cu" if c["kv"] == mi.KV_FP8 else "decode_sm103.cu"
     dec_s = dec_ms * 1e-3
     gbs = byts / dec_s / 1e9
     tflops = flops / dec_s / 1e12
@@ -417,11 +422,11 @@ def run_ours(args):
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs / peaks["hbm_gbs"], "traffic": measured_traffic(traffic_key)}
+                "frac": gbs / peaks["hbm_gbs"], "traffic": measured_traffic(traffic_key, traffic_kernel)}
     else:
         pk = peaks["bf16_tflops_sustained"]
         roof = {"bound": "tensor", "achieved": tflops, "peak": pk, "unit": "TFLOP/s", "frac": tflops / pk,
-                "traffic": measured_traffic(traffic_key)}
+                "traffic": measured_traffic(traffic_key, traffic_kernel)}
     roof.update({"kernel": "mla_decode", "peak_source": f"{peak_src} (MEASURED_PEAKS.json)",
                  "bytes_per_launch": byts, "flops_per_launch": flops,
                  "min_roofline_frac": max(t_hbm, t_tc) / dec_s})
