@@ -87,6 +87,24 @@ def test_batch_zero_and_workspace_checks():
     assert e.value.status == mla.ERR_WORKSPACE_TOO_SMALL
 
 
+@pytest.mark.parametrize("kv", [mi.KV_BF16, mi.KV_FP8])
+@pytest.mark.parametrize("num_splits", [-2, 3, 8])
+def test_many_short_units_stay_finite(kv, num_splits):
+    """Stress of the P hand-off between the two CTAs: 130 rows of 1..130 tokens (many units of
+    one or two pages, and empty splits), five calls in a row on one device buffer set. Every
+    call must match the oracle, with finite outputs everywhere and a clean device status."""
+    import torch
+    c = mi.decode_case(130, 1, 32, list(range(1, 131)), kv=kv, seed=70 + num_splits)
+    d = torch_dev(c)
+    o_ref, lse_ref = _oracle(c)
+    for _ in range(5):
+        o, lse, st = run_decode(c, num_splits, dev=d)
+        assert st == 0
+        assert np.isfinite(o).all() and np.isfinite(lse).all()
+        compare_decode(o, lse, o_ref, lse_ref, fp8=kv == mi.KV_FP8)
+    torch.cuda.synchronize()
+
+
 # ----------------------------------------------------------------------------- FP8 cache
 def _fp8_case(B, Sq, H, lens, seed, vscale=2.0):
     """FP8 cache with v_scale = vscale * k_scale, so that swapping the two scales cannot pass."""
