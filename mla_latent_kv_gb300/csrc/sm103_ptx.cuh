@@ -203,13 +203,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* gsrc, uint32
                  : "memory");
 }
 
-// Prefetch `bytes` (a multiple of 16) of contiguous global memory into L2 (no shared memory,
-// no completion tracking).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* gptr, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gptr)), "r"(bytes)
-                 : "memory");
-}
-
 // TMA store of one box from this CTA's shared memory to global memory (elements outside the
 // tensor are not written), tracked by the issuing thread's bulk async-group.
 __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int32_t x, int32_t y, int32_t z) {
@@ -249,12 +242,6 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, uint32_t 
 __device__ __forceinline__ uint2 lds_u2(uint32_t addr) {
     uint2 v;
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
-                 : "memory");
     return v;
 }
 __device__ __forceinline__ void sts_u4(uint32_t addr, uint4 v) {
@@ -342,12 +329,6 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote, uint4 v, uint32_t r
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
                      remote),
                  "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void st_async_v2(uint32_t remote, uint32_t a, uint32_t b, uint32_t remote_bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(remote),
-                 "r"(a), "r"(b), "r"(remote_bar)
                  : "memory");
 }
 
