@@ -113,9 +113,10 @@ int mla_default_num_splits(int max_seq_len, int sm_count);
 /* Effective split count mla_decode will use for a `num_splits` request on the current CUDA
  * device:  > 0  that many splits (forced);
  *            0  mla_default_num_splits(max_seq_len, SM count of the device);
- *           -1  this library's own choice for GB300: the smallest count whose grid of
- *               (B*Sq*splits) units fills whole waves of the device's SMs, capped by the
- *               number of 64-token pages of the longest row.
+ *           -1  this library's own choice for GB300, from max_seq_len alone: each of the
+ *               B*Sq*S units runs on one pair of SMs, and S minimises
+ *               waves(S) * (pages per split + a fixed per-unit cost of 8 page-times) plus the
+ *               partial states' traffic, for S up to the number of 64-token pages.
  *           -2  no uniform count: a schedule is built on the device from seq_lens (no host
  *               synchronisation, [vLLM-MLA, metadata section]: FlashMLA's decode metadata
  *               carries a scheduler plan). Every query row is cut into page-aligned units of

@@ -121,8 +121,13 @@ int mla_resolve_num_splits(int num_splits, int B, int Sq, int H, int max_seq_len
     if (sms < 1) return -1;
     if (num_splits == 0) return mla_default_num_splits(max_seq_len, sms);
     // GB300 plan: each unit (one query row x one split) occupies one pair of SMs. Estimate the
-    // time of S splits as  waves(S) * pages_per_split(S) * t_page  plus the partial-state
-    // traffic of the split path, and take the cheapest S.
+    // time of S splits as  waves(S) * (pages_per_split(S) + o) * t_page  plus the partial-state
+    // traffic of the split path, and take the cheapest S. o is a unit's fixed cost (pipeline
+    // fill, Q load, epilogue, wave tail) in page-times. Measurements of the bf16 kernel put it
+    // near 18 (one split of 64 pages: 115 us; of 228 pages: 344 us, i.e. 1.4 us per page and
+    // 25 us per unit); a smaller value is used because the host sees only max_seq_len, and a
+    // ragged batch's longest row is better split than the uniform model says.
+    constexpr double kUnitOverheadPages = 8.0;
     const int slots = std::max(1, sms / 2);
     const int64_t rows = (int64_t)B * Sq;
     const int pages = std::max(1, (max_seq_len + mla::kPage - 1) / mla::kPage);
@@ -135,7 +140,7 @@ int mla_resolve_num_splits(int num_splits, int B, int Sq, int H, int max_seq_len
         int64_t units = rows * S;
         int64_t waves = (units + slots - 1) / slots;
         int per = (pages + S - 1) / S;
-        double t = (double)waves * per * page_bytes * slots;  // bytes moved at the wave rate
+        double t = (double)waves * (per + kUnitOverheadPages) * page_bytes * slots;  // at the wave rate
         if (S > 1) t += (double)units * partial_bytes_per_unit;
         if (t < best * 0.999) {
             best = t;
