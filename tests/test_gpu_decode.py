@@ -129,6 +129,15 @@ def test_fp8_ragged_multi_page(num_splits):
     assert err["rel_l2"] <= 5e-3 and err["lse_max"] <= 1e-3, err
 
 
+@pytest.mark.parametrize("num_splits", [1, -2])  # bf16 o_latent from the FP8 kernel's epilogue / merge
+def test_fp8_bf16_output(num_splits):
+    c = _fp8_case(3, 1, 64, [5, 64, 300], seed=29)
+    o, lse, st = run_decode(c, num_splits, o_dtype=1)
+    o_ref, lse_ref = _oracle(c)
+    assert st == 0
+    compare_decode(o, lse, o_ref, lse_ref, fp8=True, extra_abs=float(np.abs(o_ref).max()) * 2.0 ** -9)
+
+
 def test_fp8_causal_two_rows_and_heads():
     c = _fp8_case(3, 2, 20, [0, 2, 333], seed=27, vscale=0.5)
     o, lse, st = run_decode(c, 2)
