@@ -123,7 +123,7 @@ enum : int {
     B_VRAWEMPTY = B_VRAWFULL + kVRawSlots,  // [kVRawSlots] CTA1: raw half page widened (256)
     B_VFULL = B_VRAWEMPTY + kVRawSlots,  // [kVStages] CTA1: V stage written (256 converter threads)
     B_VEMPTY = B_VFULL + kVStages,       // [kVStages] CTA1: V stage consumed
-    B_PFULL = B_VEMPTY + kVStages,       // [kPBufs] CTA1: P message landed (st.async bytes from CTA0)
+    B_PFULL = B_VEMPTY + kVStages,       // [kPBufs] CTA1: P message landed (bulk copy bytes from CTA0)
     B_READY = B_PFULL + kPBufs,          // [kPBufs] CTA1: O rescaled for the page (128 helper threads)
     B_STATS = B_READY + kPBufs,          // CTA1: final row statistics written by CTA0
     B_STAGEFREE,                         // [2] CTA0: a half's last P message has landed in CTA 1

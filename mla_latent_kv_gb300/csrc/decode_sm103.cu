@@ -12,7 +12,7 @@
 //
 //   CTA 0 ("scores")  Q: the 512 latent dims (128 heads x 512 bf16) are loaded once by TMA and
 //                     kept in tensor memory; the 64 rope dims stay in shared memory.
-//                     K: a ring of six 32 KB slots, one slot = one 64-dim panel of a group's
+//                     K: a ring of four 32 KB slots, one slot = one 64-dim panel of a group's
 //                     four pages (256 rows, 128-byte swizzle), refilled panel by panel by TMA as
 //                     the MMAs release them.
 //                     S = Q K^T per group: 36 tcgen05.mma of M=128 heads x N=256 tokens x K=16
@@ -21,9 +21,13 @@
 //                     Softmax: eight warps, two per TMEM lane quarter, each owning two pages of
 //                     the group for 32 heads; fp32 online softmax with a lazily moved running
 //                     max (rescale only when a row's max grows by more than 2^8). Each thread
-//                     stores its head's P row (bf16, in the MMA's swizzled K-major layout) and
-//                     rescale factor straight into CTA 1's P buffer for the page with st.async,
-//                     whose bytes are counted on CTA 1's barrier for that buffer.
+//                     writes its head's P row (bf16, in the MMA's swizzled K-major layout) and
+//                     rescale factor into a local staging buffer for the page (one of four, one
+//                     per page of the group); one thread per half then sends the whole buffer
+//                     to CTA 1's P buffer for the page with a single bulk copy, whose bytes
+//                     complete CTA 1's barrier for that buffer. One bulk copy moves the 17 KB
+//                     about twice as fast as 128 threads' st.async stores, and the softmax
+//                     warps are free as soon as their shared-memory writes are done.
 //   CTA 1 ("output")  holds the 128 x 512 fp32 output accumulator -- all 512 TMEM columns of its
 //                     SM, the reason the work is split over two SMs -- streams the pages'
 //                     first 512 dims (mostly L2 hits), and accumulates O += P V per page with
@@ -59,7 +63,7 @@ using namespace dec;
 
 constexpr int kThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (CTA 0) / 2-5 helpers, 2-9 epilogue (CTA 1)
 constexpr int kPPG = 4;              // pages per group
-constexpr int kSlots = 6;            // CTA 0 K ring slots (32 KB each)
+constexpr int kSlots = 4;            // CTA 0 K ring slots (32 KB each)
 constexpr int kPageBox = 64 * 128;   // one page's rows of one 64-dim panel (8 KB)
 constexpr int kSlotBytes = kPPG * kPageBox;  // 32 KB
 constexpr int kQPanelBytes = 128 * 128;      // 128 heads x 64 dims of Q (16 KB)
@@ -70,13 +74,14 @@ constexpr int kVPerPage = kPage / kVRows;        // V stages per page
 constexpr int kVBox = kVRows * 128;             // one 64-dim panel of a V stage (8 KB)
 constexpr int kVStageBytes = 8 * kVBox;         // 64 KB
 constexpr int kPBytes = 128 * 128;              // P page: 128 heads x 64 tokens bf16
-constexpr int kPMsgBytes = kPBytes + 512 + 4;   // P + alpha[128] + flag word, stored by st.async
+constexpr int kPMsgBytes = (kPBytes + 512 + 4 + 15) / 16 * 16;  // P + alpha[128] + flag word, in 16-byte units
 constexpr int kPBufStride = 17 * 1024;
 constexpr int kCtrlBytes = 4096;
 // CTA 0 layout
 constexpr int OFF_QROPE = kCtrlBytes;                      // 16 KB
-constexpr int OFF_RING = OFF_QROPE + kQPanelBytes;         // 6 x 32 KB
-constexpr int kSmem0 = OFF_RING + kSlots * kSlotBytes;
+constexpr int OFF_RING = OFF_QROPE + kQPanelBytes;         // 4 x 32 KB
+constexpr int OFF_STAGE = OFF_RING + kSlots * kSlotBytes;  // 4 P staging buffers, kPBufStride apart
+constexpr int kSmem0 = OFF_STAGE + 4 * kPBufStride;
 // CTA 1 layout
 constexpr int OFF_V = kCtrlBytes;
 constexpr int OFF_PB = OFF_V + kVStages * kVStageBytes;
@@ -84,14 +89,17 @@ constexpr int kSmem1 = OFF_PB + kPBufs * kPBufStride;
 constexpr int kSmemBytes = kSmem0 > kSmem1 ? kSmem0 : kSmem1;
 static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
 static_assert(kPMsgBytes <= kPBufStride, "P message");
-// Q's latent panels land in ring slots 2-5, so that the first K panels can load into slots 0
-// and 1 at once.
-static_assert(8 * kQPanelBytes == 4 * kSlotBytes && kSlots >= 6, "Q panel homes");
-static_assert(OFF_RING % 1024 == 0 && OFF_PB % 1024 == 0 && kPBufStride % 1024 == 0 && kVBox % 1024 == 0,
+// Q's latent panels land in the four staging buffers (panels 0-3) and ring slots 2-3 (panels
+// 4-7), so that the first K panels can load into slots 0 and 1 at once; P is staged only after
+// the first S, which needs Q in tensor memory.
+static_assert(kSlots == 4 && kPBufStride >= kQPanelBytes && 4 * kQPanelBytes == 2 * kSlotBytes, "Q panel homes");
+static_assert(OFF_RING % 1024 == 0 && OFF_STAGE % 1024 == 0 && OFF_PB % 1024 == 0 && kPBufStride % 1024 == 0 && kVBox % 1024 == 0,
               "128-byte swizzled tiles need 1024-byte alignment");
 // the epilogue stages its output tiles over the V ring and the P buffers
 static_assert(OFF_V + 8 * 128 * 128 <= kSmem1, "epilogue tiles");
-__device__ __forceinline__ uint32_t q_panel_off(int pn) { return OFF_RING + 2 * kSlotBytes + pn * kQPanelBytes; }
+__device__ __forceinline__ uint32_t q_panel_off(int pn) {
+    return pn < 4 ? OFF_STAGE + pn * kPBufStride : OFF_RING + 2 * kSlotBytes + (pn - 4) * kQPanelBytes;
+}
 
 // Barrier slots (8 bytes each); one layout for both CTAs so that a multicast commit from CTA 1
 // lands on CTA 0's B_PEMPTY slots.
@@ -105,10 +113,11 @@ enum : int {
     B_PEMPTY,                          // [kPBufs] both CTAs: PV MMA of the page in P buffer b completed
     B_VFULL = B_PEMPTY + kPBufs,       // [kVStages] CTA1: V stage landed
     B_VEMPTY = B_VFULL + kVStages,     // [kVStages] CTA1: V stage consumed
-    B_PFULL = B_VEMPTY + kVStages,     // [kPBufs] CTA1: P message landed (st.async bytes from CTA0)
+    B_PFULL = B_VEMPTY + kVStages,     // [kPBufs] CTA1: P message landed (bulk copy bytes from CTA0)
     B_READY = B_PFULL + kPBufs,        // [kPBufs] CTA1: page ready for its PV MMA (128 helper threads)
     B_STATS = B_READY + kPBufs,        // CTA1: final row statistics written by CTA0 (one cluster-scope arrive)
-    B_COUNT
+    B_STAGEFREE,                       // [4] CTA0: staging buffer's copy has landed (remote arrive from CTA1)
+    B_COUNT = B_STAGEFREE + 4
 };
 static_assert(8 * B_COUNT <= 512, "barrier slots");
 constexpr int OFF_TMEM = 512;
@@ -124,6 +133,7 @@ constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 256, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kBarMax = 1, kBarOr = 2, kBarHalf0 = 3;  // named barriers of the softmax warps
+constexpr uint32_t kBarStage0 = 5;                          // [2] one per softmax half: P staged
 constexpr uint32_t kBarEpi = 4;                             // named barrier of CTA 1's helper warps
 constexpr int kEpiPanelBytes = 128 * 128;                   // 128 rows x 128 B output tile
 
@@ -208,7 +218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             tma_load_2d(sbase + OFF_QROPE, &q_map, bar(B_QFULL), 8 * 64, g.r * p.H);
                             q_issued = true;
                         }
-                        // first use of slots 2-5: Q's panels have been moved out to TMEM
+                        // first use of slots 2-3: Q's panels have been moved out to TMEM
                         ok = k > 0      ? wait_bar(bar(B_SLOTEMPTY + slot), (k - 1) & 1, abort, ds)
                              : slot >= 2 ? wait_bar(bar(B_QREADY), 0, abort, ds)
                                          : true;
@@ -371,22 +381,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         l_run += (bf16_lo_f(pk[c]) + bf16_hi_f(pk[c])) +
                                  (bf16_lo_f(pk[16 + c]) + bf16_hi_f(pk[16 + c]));
                     }
-                    if (page < npages && okS) {
-                        // CTA 1's buffer for this page is free once the PV of the page kPBufs
-                        // earlier has completed (multicast commit)
-                        const int pb = page % kPBufs, up = page / kPBufs;
-                        if (up > 0 && !warp_wait<true>(bar(B_PEMPTY + pb), (up - 1) & 1, abort, ds)) continue;
-                        const uint32_t dst = pbuf_remote + pb * kPBufStride;
-                        const uint32_t fb = pfull_remote + 8u * pb;
+                    {
+                        // staging buffer sbi takes page sbi of every group; it is free again once
+                        // the previous group's copy out of it has landed in CTA 1
+                        const int sbi = 2 * half + q;
+                        const int htid = tid - 64 - 128 * half;
+                        uint8_t* stage = smem + OFF_STAGE + sbi * kPBufStride;
+                        if (page < npages) {  // pages past the end send nothing and leave the buffer alone
+                            if (gi > 0) warp_wait<true>(bar(B_STAGEFREE + sbi), (gi - 1) & 1, abort, ds);
 #pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            st_async_v4(dst + row * 128 + ((c ^ (row & 7)) << 4),
-                                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]), fb);
-                        // every page carries the group's rescale factors; the group's first page
-                        // also carries the flag that tells CTA 1 to rescale O first
-                        st_async_b32(dst + kPBytes + 4 * row, __float_as_uint(alpha), fb);
-                        if (row == 0)
-                            st_async_b32(dst + kPBytes + 512, (half == 0 && q == 0 && any) ? 1u : 0u, fb);
+                            for (int c = 0; c < 8; ++c)
+                                *reinterpret_cast<uint4*>(stage + row * 128 + ((c ^ (row & 7)) << 4)) =
+                                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                            // every page carries the group's rescale factors; the group's first
+                            // page also carries the flag that tells CTA 1 to rescale O first
+                            reinterpret_cast<float*>(stage + kPBytes)[row] = alpha;
+                            if (row == 0)
+                                *reinterpret_cast<uint32_t*>(stage + kPBytes + 512) = (half == 0 && q == 0 && any) ? 1u : 0u;
+                            fence_proxy_async_cta();  // generic writes before the bulk copy reads them
+                        }
+                        named_bar(kBarStage0 + half, 128);
+                        if (htid == 0 && page < npages && okS) {
+                            // CTA 1's buffer for this page is free once the PV of the page kPBufs
+                            // earlier has completed (multicast commit)
+                            const int pb = page % kPBufs, up = page / kPBufs;
+                            if (up == 0 || wait_bar<true>(bar(B_PEMPTY + pb), (up - 1) & 1, abort, ds))
+                                bulk_copy_to_peer(pbuf_remote + pb * kPBufStride,
+                                                  sbase + OFF_STAGE + sbi * kPBufStride, kPMsgBytes,
+                                                  pfull_remote + 8u * pb);
+                        }
                     }
                 }
             }
@@ -454,7 +477,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 bool ok = true;
                 for (int i = 0; i < npages && ok; ++i) {
                     const int pb = i % kPBufs;
-                    // V and P were written by the async proxy (TMA / st.async): the MMA thread
+                    // V and P were written by the async proxy (TMA / bulk copy): the MMA thread
                     // observes their barriers itself; READY adds the helpers' rescale / zeroing.
                     if (!(ok = wait_bar(bar(B_PFULL + pb), (i / kPBufs) & 1, abort, ds))) break;
                     if (!(ok = wait_bar(bar(B_READY + pb), (i / kPBufs) & 1, abort, ds))) break;
@@ -500,7 +523,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int i = 0; i < npages && warp < 6; ++i) {
                 const int pb = i % kPBufs, up = i / kPBufs;
                 if (!warp_wait(bar(B_PFULL + pb), up & 1, abort, ds)) break;
-                if (ctid == 0) bar_arrive_expect_tx(bar(B_PFULL + pb), kPMsgBytes);  // re-arm for the next message
+                if (ctid == 0) {
+                    bar_arrive_expect_tx(bar(B_PFULL + pb), kPMsgBytes);  // re-arm for the next message
+                    bar_arrive_remote(bar(B_STAGEFREE + (i & 3)), 0);     // CTA 0's staging buffer is free
+                }
                 const uint8_t* pmsg = smem + OFF_PB + pb * kPBufStride;
                 const bool fix = i > 0 && *reinterpret_cast<const volatile uint32_t*>(pmsg + kPBytes + 512) != 0;
                 const int valid = valid_rows(g, i);

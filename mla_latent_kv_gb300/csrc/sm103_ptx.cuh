@@ -322,22 +322,6 @@ __device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_
         : "memory");
 }
 
-// Asynchronous stores into the other CTA's shared memory: `remote` and `remote_bar` are
-// shared::cluster addresses in the same CTA; the stored bytes are counted (complete_tx) on that
-// barrier.
-__device__ __forceinline__ void st_async_v4(uint32_t remote, uint4 v, uint32_t remote_bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                     remote),
-                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void st_async_b32(uint32_t remote, uint32_t v, uint32_t remote_bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote), "r"(v),
-                 "r"(remote_bar)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
