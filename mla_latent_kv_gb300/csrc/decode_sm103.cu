@@ -34,7 +34,9 @@
 //                     tcgen05.mma (M=128, N=2x256, K=64; V read as an MN-major operand straight
 //                     from the TMA tile). Its MMA thread waits for P, the helpers and V; four
 //                     helper warps re-arm the P buffers, rescale O, zero the V rows past the
-//                     last token, and (with four more warps) run the epilogue.
+//                     last token, and (with four more warps) run the epilogue. Until the
+//                     epilogue those four other warps prefetch into L2 the pages that CTA 0
+//                     will load about one group later, so that its K loads hit L2.
 // Per page the pair issues exactly the algorithm's 2*128*64*(576+512) flops.
 //
 // Rows past the split's last visible token are masked by index (S = -inf) and, in the last
@@ -60,6 +62,17 @@ namespace {
 
 using namespace ptx;
 using namespace dec;
+
+// Hint: bring the 128-byte line at `ptr` into L2 (no effect on correctness).
+__device__ __forceinline__ void prefetch_l2(const void* ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
+
+// A 32-bit global load through the non-coherent path, issued where it stands in program order
+// (the asm is volatile), for data that no kernel of the grid writes.
+__device__ __forceinline__ int ld_nc_s32(const int32_t* ptr) {
+    int v;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
+    return v;
+}
 
 constexpr int kThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (CTA 0) / 2-5 helpers, 2-9 epilogue (CTA 1)
 constexpr int kPPG = 4;              // pages per group
@@ -122,6 +135,7 @@ enum : int {
 static_assert(8 * B_COUNT <= 512, "barrier slots");
 constexpr int OFF_TMEM = 512;
 constexpr int OFF_ABORT = 516;
+constexpr int OFF_PROG = 520;     // CTA1: pages made ready by the helper warps (paces the L2 prefetch)
 constexpr int OFF_MX = 1024;       // CTA0: f32 [2][128] exchange between the two warp halves
 constexpr int OFF_STAT_M = 2048;   // CTA1: f32 [128] final running max (log2 units)
 constexpr int OFF_STAT_L = 2560;   // CTA1: f32 [128] row sum of the bf16-rounded P (normalises O)
@@ -136,6 +150,7 @@ constexpr uint32_t kBarMax = 1, kBarOr = 2, kBarHalf0 = 3;  // named barriers of
 constexpr uint32_t kBarStage0 = 5;                          // [2] one per softmax half: P staged
 constexpr uint32_t kBarEpi = 4;                             // named barrier of CTA 1's helper warps
 constexpr int kEpiPanelBytes = 128 * 128;                   // 128 rows x 128 B output tile
+constexpr int kPrefetchAhead = 8;  // pages (two groups) between the helpers' progress and the page prefetched into L2
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_sm103_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap kvh_map,
@@ -157,6 +172,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         griddep_wait();
         if (unit >= *p.plan_count) return;
     }
+    // The first split of a row starts at page 0 whatever the row's length, so the K producer
+    // fetches the first group's block-table entries while the length is still on its way
+    // (validated once the page count is known).
+    int blk_early[kPPG] = {-1, -1, -1, -1};
+    const bool early_blocks = p.plan_units == nullptr && p.qsl == nullptr && unit % p.num_splits == 0;
+    if (early_blocks && tid == 0 && rank == 0) {
+        const int32_t* row = p.block_table + (size_t)(unit / p.num_splits / p.Sq) * p.max_blocks;
+#pragma unroll
+        for (int q = 0; q < kPPG; ++q)
+            if (q < p.max_blocks) blk_early[q] = ld_nc_s32(row + q);
+    }
     const RowGeom g = row_geometry(p, unit, tid == 0 && rank == 0);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
     int32_t* ds = p.dev_status;
@@ -166,6 +192,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         *abort = 0;
+        *reinterpret_cast<volatile int*>(smem + OFF_PROG) = 0;
         for (int i = 0; i < B_COUNT; ++i) {
             uint32_t cnt = 1;
             if (i == B_SEMPTY || i == B_QREADY) cnt = 256;
@@ -191,33 +218,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ============================== scores CTA ==============================
         if (warp == 0) {
             if (lane == 0 && npages > 0) {
-                tma_prefetch_desc(&q_map);
                 tma_prefetch_desc(&kv_map);
-                // The first K panels go out before the preceding kernel (which may be writing q)
-                // has finished: no kernel of this library writes the cache. No L2 prefetch: the
-                // SM's TMA unit is the narrow point of the K stream, and bulk prefetches issued
-                // through it delay the ring's own loads.
+                // The K panels go out before the preceding kernel (which may be writing q) has
+                // finished: no kernel of this library writes the cache. CTA 1 prefetches the
+                // pages into L2 ahead of these loads, with plain prefetch instructions: bulk
+                // prefetches issued here would queue in this SM's TMA unit, the narrow point of
+                // the K stream.
                 const int oob = (int)(p.num_blocks * kPage);  // one past the cache: TMA fills zeros
-                bool q_issued = false;
                 int issued = 0;  // K panels issued
                 bool ok = true;
                 for (int gi = 0; gi < ngroups && ok; ++gi) {
                     int y[kPPG];
                     const int np = min(kPPG, npages - kPPG * gi);
                     for (int q = 0; q < np; ++q) {
-                        const int blk = page_block(p, g.b, g.page0 + kPPG * gi + q);
+                        int blk;
+                        if (gi == 0 && early_blocks) {  // the entry fetched early: same checks as page_block
+                            blk = blk_early[q];
+                            if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+                                if (p.dev_status) atomicOr(p.dev_status, MLA_DEV_BAD_BLOCK_ID);
+                                blk = -1;
+                            }
+                        } else {
+                            blk = page_block(p, g.b, g.page0 + kPPG * gi + q);
+                        }
                         y[q] = blk < 0 ? oob : blk * kPage;
                     }
                     for (int pn = 0; pn < 9; ++pn) {
                         const int m = 9 * gi + pn, slot = m % kSlots, k = m / kSlots;
-                        if (!q_issued && m == 2) {  // Q: the preceding kernel's output
-                            griddep_wait();
-                            bar_arrive_expect_tx(bar(B_QFULL), 9 * kQPanelBytes);
-                            for (int qn = 0; qn < 8; ++qn)
-                                tma_load_2d(sbase + q_panel_off(qn), &q_map, bar(B_QFULL), qn * 64, g.r * p.H);
-                            tma_load_2d(sbase + OFF_QROPE, &q_map, bar(B_QFULL), 8 * 64, g.r * p.H);
-                            q_issued = true;
-                        }
                         // first use of slots 2-3: Q's panels have been moved out to TMEM
                         ok = k > 0      ? wait_bar(bar(B_SLOTEMPTY + slot), (k - 1) & 1, abort, ds)
                              : slot >= 2 ? wait_bar(bar(B_QREADY), 0, abort, ds)
@@ -232,7 +259,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (*abort) {  // let the copies in flight land before the CTA can exit
                     volatile int dummy = 0;
-                    if (q_issued) wait_bar(bar(B_QFULL), 0, &dummy, nullptr);
                     for (int m = (issued > kSlots ? issued - kSlots : 0); m < issued; ++m) {
                         dummy = 0;
                         wait_bar(bar(B_SLOTFULL + m % kSlots), (m / kSlots) & 1, &dummy, nullptr);
@@ -241,6 +267,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
         } else if (warp == 1) {
             if (lane == 0 && npages > 0) {
+                // Q, the preceding kernel's output, is loaded from here so that it goes out at
+                // once, in parallel with the producer's block-table reads and first K panels.
+                tma_prefetch_desc(&q_map);
+                griddep_wait();
+                bar_arrive_expect_tx(bar(B_QFULL), 9 * kQPanelBytes);
+                for (int qn = 0; qn < 8; ++qn)
+                    tma_load_2d(sbase + q_panel_off(qn), &q_map, bar(B_QFULL), qn * 64, g.r * p.H);
+                tma_load_2d(sbase + OFF_QROPE, &q_map, bar(B_QFULL), 8 * 64, g.r * p.H);
                 int done = 0;
                 bool ok = wait_bar(bar(B_QREADY), 0, abort, ds);
                 if (ok) tc_fence_after();
@@ -274,6 +308,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int m = (done > kSlots ? done - kSlots : 0); m < done; ++m) {
                     dummy = 0;
                     wait_bar(bar(B_SLOTEMPTY + m % kSlots), (m / kSlots) & 1, &dummy, nullptr);
+                }
+                if (*abort) {  // and Q has landed
+                    dummy = 0;
+                    wait_bar(bar(B_QFULL), 0, &dummy, nullptr);
                 }
             }
         } else {
@@ -566,6 +604,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 bar_arrive(bar(B_READY + pb));
                 pages_ready = i + 1;
+                if (ctid == 0) *reinterpret_cast<volatile int*>(smem + OFF_PROG) = pages_ready;
+            }
+            if (warp >= 6 && npages > kPPG) {
+                // Warps 6-9 have nothing to do until the epilogue: they prefetch into L2 the page
+                // kPrefetchAhead pages past the helpers' progress, which is about one group past
+                // the page the scores CTA's K producer loads, so that its TMA loads hit L2. Plain
+                // prefetch instructions, not bulk prefetches: those would queue in the TMA unit.
+                // Only a hint: the loop gives up quietly if it falls behind or the unit aborts.
+                const int ptid = tid - 192;
+                const volatile int* prog = reinterpret_cast<const volatile int*>(smem + OFF_PROG);
+                const int32_t* brow = p.block_table + (size_t)g.b * p.max_blocks + g.page0;
+                int spins = 0;
+                for (int t = kPPG; t < npages; ++t) {
+                    bool go = true;
+                    while (*prog < t - kPrefetchAhead) {
+                        if (*abort || ++spins > (1 << 20)) {
+                            go = false;
+                            break;
+                        }
+                        __nanosleep(128);
+                    }
+                    if (!go) break;
+                    const int32_t blk = brow[t];
+                    if (blk < 0 || (int64_t)blk >= p.num_blocks) continue;
+                    const uint8_t* page = p.cache + (size_t)blk * (kPage * kBf16RowBytes);
+                    for (int l = ptid; l < kPage * kBf16RowBytes / 128; l += 128) prefetch_l2(page + 128 * l);
+                }
             }
             // epilogue (outputs may still be read by the preceding kernel until it completes)
             griddep_wait();
