@@ -113,8 +113,10 @@ int mla_default_num_splits(int max_seq_len, int sm_count);
 /* Effective split count mla_decode will use for a `num_splits` request on the current CUDA
  * device:  > 0  that many splits (forced);
  *            0  mla_default_num_splits(max_seq_len, SM count of the device);
- *           -1  this library's own choice for GB300, from max_seq_len alone: each of the
- *               B*Sq*S units runs on one pair of SMs, and S minimises
+ *           -1  this library's own choice for GB300. With more query rows (B*Sq) than SM
+ *               pairs the units run in several waves whose packing depends on the rows'
+ *               lengths, so -1 resolves to -2 (returned as -2). Otherwise, from max_seq_len
+ *               alone: each of the B*Sq*S units runs on one pair of SMs, and S minimises
  *               waves(S) * (pages per split + a fixed per-unit cost of 8 page-times) plus the
  *               partial states' traffic, for S up to the number of 64-token pages.
  *           -2  no uniform count: a schedule is built on the device from seq_lens (no host
@@ -122,7 +124,7 @@ int mla_default_num_splits(int max_seq_len, int sm_count);
  *               carries a scheduler plan). Every query row is cut into page-aligned units of
  *               about c pages, with c chosen from the total and longest row lengths by a model
  *               of how the device's 2-SM clusters run the units; a row that gets one unit writes
- *               its output directly. For batches whose lengths differ widely. Returned as -2.
+ *               its output directly. Returned as -2.
  * Returns -1 on invalid arguments or if the SM count cannot be queried. Host only, no sync. */
 int mla_resolve_num_splits(int num_splits, int B, int Sq, int H, int max_seq_len);
 
@@ -130,7 +132,7 @@ int mla_resolve_num_splits(int num_splits, int B, int Sq, int H, int max_seq_len
  * num_splits == 1, else B*Sq*num_splits*H*(512 + 1)*4 rounded up to 256 (fp32 partial outputs
  * and partial LSEs, [vLLM-MLA, Triton MLA section]: attn_logits (B, N, splits, 512 + 1), fp32
  * because the LSE precision decides the merge). num_splits == -2 (device-built schedule): the
- * schedule (256 B + 16 B per unit + 8 B per query row) and partials for B*Sq + SMs units, each
+ * schedule (256 B + 16 B per unit + 12 B per query row) and partials for B*Sq + SMs units, each
  * region 256-byte aligned. Host only. */
 size_t mla_decode_workspace_bytes(int B, int Sq, int H, int num_splits);
 

@@ -172,18 +172,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         return;  // both CTAs of the cluster see the same alignment and leave together
     }
     const int unit = (int)(blockIdx.x >> 1);
-    if (p.plan_units) {
-        // the schedule is the preceding kernel's output; clusters past its unit count leave
-        // together (both CTAs read the same count) before touching anything
-        griddep_wait();
-        if (unit >= *p.plan_count) return;
-    }
-    const RowGeom g = row_geometry(p, unit, tid == 0 && rank == 0);
+    RowGeom g{};
+    if (!p.plan_units) g = row_geometry(p, unit, tid == 0 && rank == 0);  // its loads overlap the set-up
     volatile int* abort = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
     int32_t* ds = p.dev_status;
     auto bar = [&](int i) -> uint32_t { return sbase + OFF_CTRL + 8u * (uint32_t)i; };
-    const int npages = g.npages;
-    const int ngroups = (npages + kPPG - 1) / kPPG;
 
     if (tid == 0) {
         *abort = 0;
@@ -211,6 +204,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();  // both CTAs' barriers exist before any remote arrive or store
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM);
     if (tid == 0) griddep_launch_dependents();
+    if (p.plan_units) {
+        // The schedule is the preceding kernel's output: the set-up above overlapped it.
+        // Clusters past its unit count leave together (both CTAs read the same count).
+        griddep_wait();
+        if (unit >= *p.plan_count) {
+            if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+            cluster_sync();
+            return;
+        }
+        g = row_geometry(p, unit, tid == 0 && rank == 0);
+    }
+    const int npages = g.npages;
+    const int ngroups = (npages + kPPG - 1) / kPPG;
 
     if (rank == 0) {
         // ============================== scores CTA ==============================

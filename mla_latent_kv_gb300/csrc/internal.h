@@ -43,7 +43,8 @@ struct DecodeArgs {
     // [rows[r].x, rows[r].x + rows[r].y) when rows[r].y > 1. Null in the uniform-split modes.
     const int4* plan_units;
     const int2* plan_rows;
-    const int* plan_count;      // number of units actually planned
+    const int* plan_count;      // [0] units actually planned, [1] split rows (rows with partials)
+    const int* plan_split_rows; // the split rows' indices, plan_count[1] of them
     int plan_max_units;         // the grid is sized for this many units
 };
 

@@ -26,13 +26,14 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(DecodeArgs p) {
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();  // the partials are the preceding kernel's output
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int64_t n_tasks = (int64_t)p.rows * p.H * 2;
-    // grid-stride over (row, head, half); with a device-built schedule most rows have no
-    // partials and their tasks are skipped after one load
+    // grid-stride over (row, head, half) of the rows with partials: every row with uniform
+    // splits, the listed split rows with a device-built schedule (none: the kernel ends here)
+    const int64_t n_rows = p.plan_rows ? (int64_t)p.plan_count[1] : (int64_t)p.rows;
+    const int64_t n_tasks = n_rows * p.H * 2;
     for (int64_t t = (int64_t)blockIdx.x * kWarps + warp; t < n_tasks; t += (int64_t)gridDim.x * kWarps) {
         const int64_t item = t >> 1;
-        const int64_t r = item / p.H;
-        if (p.plan_rows && p.plan_rows[r].y <= 1) continue;  // the row wrote its output directly
+        const int64_t i = item / p.H;
+        const int64_t r = p.plan_rows ? (int64_t)p.plan_split_rows[i] : i;
         merge_item(p, r, (int)(item % p.H), (int)(t & 1), lane);
     }
 }
@@ -114,7 +115,7 @@ __device__ __forceinline__ void merge_item(const DecodeArgs& p, int64_t r, int h
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
     const int64_t n_tasks = (int64_t)a.rows * a.H * 2;
     int64_t blocks = (n_tasks + kWarps - 1) / kWarps;
-    if (a.plan_rows && blocks > 1216) blocks = 1216;  // grid-stride; the split rows are few
+    if (a.plan_rows && blocks > 304) blocks = 304;  // grid-stride over the split rows, which are few
     return launch_pdl(merge_kernel, dim3((unsigned)blocks), dim3(kWarps * 32), 0, s, a);
 }
 

@@ -60,7 +60,7 @@ WorkspaceLayout workspace_layout(int kv_dtype, int B, int64_t rows, int H, int n
         if (sms < 1) return w;
         slots = plan_max_units(rows, sms / 2 > 0 ? sms / 2 : 1);
         w.plan = 0;
-        off = up(256 + (size_t)slots * sizeof(int4)) + up((size_t)rows * sizeof(int2));
+        off = up(256 + (size_t)slots * sizeof(int4)) + up((size_t)rows * sizeof(int2)) + up((size_t)rows * sizeof(int));
     }
     if (slots > 0) {
         const size_t units = (size_t)slots * H;
@@ -120,6 +120,9 @@ int mla_resolve_num_splits(int num_splits, int B, int Sq, int H, int max_seq_len
     int sms = device_sm_count();
     if (sms < 1) return -1;
     if (num_splits == 0) return mla_default_num_splits(max_seq_len, sms);
+    // More query rows than SM pairs: the units run in several waves, and how they pack depends on
+    // the rows' lengths, which only the device has. -1 then builds the schedule there (as -2).
+    if ((int64_t)B * Sq > std::max(1, sms / 2)) return -2;
     // GB300 plan: each unit (one query row x one split) occupies one pair of SMs. Estimate the
     // time of S splits as  waves(S) * (pages_per_split(S) + o) * t_page  plus the partial-state
     // traffic of the split path, and take the cheapest S. o is a unit's fixed cost (pipeline
@@ -265,7 +268,9 @@ mla_status decode_impl(const void* q, const void* kv_cache, mla_kv_dtype kv_dtyp
         char* base = (char*)workspace + wl.plan;
         a.plan_count = (const int*)base;
         a.plan_units = (const int4*)(base + 256);
-        a.plan_rows = (const int2*)(base + (256 + (size_t)max_units * sizeof(int4) + 255) / 256 * 256);
+        const size_t rows_off = (256 + (size_t)max_units * sizeof(int4) + 255) / 256 * 256;
+        a.plan_rows = (const int2*)(base + rows_off);
+        a.plan_split_rows = (const int*)(base + rows_off + ((size_t)rows * sizeof(int2) + 255) / 256 * 256);
         a.plan_max_units = (int)max_units;
     }
     const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3_SCALED;

@@ -221,6 +221,90 @@ def test_device_schedule_bf16_output_and_one_long_row():
     compare_decode(o, lse, o_ref, lse_ref, extra_abs=float(np.abs(o_ref).max()) * 2.0 ** -9)
 
 
+def _up256(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("lens,Sq", [
+    ("loguniform", 1),                      # the ragged workload's length mix
+    ([4096] * 64, 1),                       # uniform: one unit per row
+    ([131072] * 4, 2),                      # few long rows: every row split evenly
+    ([20000, 5, 64, 65, 300, 1], 1),        # one long row among short ones
+    ([1 + (7 * i) % 500 for i in range(1100)], 1),  # more rows than the planner's threads
+    ([0, 0, 64, 0], 1),                     # empty rows
+])
+def test_device_schedule_is_a_partition(lens, Sq):
+    """The schedule that num_splits = -2 builds on the device, read back from the workspace: every
+    query row's visible tokens [0, n) are covered by its units exactly once and in order, the
+    partial slots are distinct, split rows are listed exactly once and their units come first."""
+    import torch
+    import mla_latent_kv_gb300 as mla
+    rng = np.random.default_rng(5)
+    if lens == "loguniform":
+        lens = [int(x) for x in np.exp(rng.uniform(0, np.log(32768), 128))]
+    B, H = len(lens), 16
+    ml = max(max(lens), 1)
+    mb = (ml + 63) // 64
+    dev = torch.device("cuda")
+    q = torch.zeros((B, Sq, H, 576), dtype=torch.bfloat16, device=dev)
+    cache = torch.zeros((1, 64 * 1152), dtype=torch.uint8, device=dev)  # every page is block 0
+    bt = torch.zeros((B, mb), dtype=torch.int32, device=dev)
+    sl = torch.tensor(lens, dtype=torch.int32, device=dev)
+    ws = torch.zeros(mla.workspace_bytes(B, Sq, H, -2, mla.KV_BF16, ml), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    mla.decode(q, cache, bt, sl, ml, 0.1, num_splits=-2, workspace=ws, dev_status=st, num_blocks=1)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    w = ws.cpu().numpy()
+    rows = B * Sq
+    pairs = max(1, torch.cuda.get_device_properties(0).multi_processor_count // 2)
+    max_units = rows + 2 * pairs
+    count, n_split = (int(x) for x in w[:8].view(np.int32))
+    assert 0 < count <= max_units and 0 <= n_split <= rows
+    units = w[256:256 + 16 * count].view(np.int32).reshape(count, 4)
+    rows_off = _up256(256 + max_units * 16)
+    row_info = w[rows_off:rows_off + 8 * rows].view(np.int32).reshape(rows, 2)
+    split_off = rows_off + _up256(rows * 8)
+    split_rows = w[split_off:split_off + 4 * n_split].view(np.int32)
+    assert np.all((units[:, 0] >= 0) & (units[:, 0] < rows))
+    slots = units[units[:, 3] >= 0, 3]
+    assert len(np.unique(slots)) == len(slots) and np.all(slots < max_units)
+    # units of split rows (those with partial slots) come first
+    has_slot = units[:, 3] >= 0
+    first_unsplit = count if has_slot.all() else int(np.argmin(has_slot))
+    assert has_slot[:first_unsplit].all() and not has_slot[first_unsplit:].any()
+    for r in range(rows):
+        b, t = divmod(r, Sq)
+        n = max(0, lens[b] - (Sq - 1 - t))
+        mine = units[units[:, 0] == r]
+        slot0, S = (int(x) for x in row_info[r])
+        assert len(mine) == S >= 1
+        mine = mine[np.argsort(mine[:, 1], kind="stable")]
+        assert mine[0, 1] == 0 and mine[-1, 2] == n
+        assert np.all(mine[:, 1] <= mine[:, 2])
+        assert np.all(mine[1:, 1] == mine[:-1, 2])
+        if S > 1:
+            assert sorted(mine[:, 3].tolist()) == list(range(slot0, slot0 + S))
+        else:
+            assert slot0 == -1 and mine[0, 3] == -1
+    split_expected = sorted(r for r in range(rows) if row_info[r, 1] > 1)
+    assert sorted(split_rows.tolist()) == split_expected
+
+
+def test_default_split_choice_uses_the_device_schedule_for_many_rows():
+    """num_splits = -1: with more query rows than SM pairs the units run in waves whose packing
+    depends on the lengths, so the library builds the schedule on the device (-2); with fewer
+    rows the host's uniform split stands."""
+    import torch
+    import mla_latent_kv_gb300 as mla
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    assert mla.resolve_num_splits(-1, pairs + 1, 1, 128, 32768) == -2
+    assert mla.resolve_num_splits(-1, (pairs + 2) // 2, 2, 128, 4096) == -2
+    assert mla.resolve_num_splits(-1, 64, 1, 128, 4096) == 1
+    assert mla.resolve_num_splits(-1, 4, 2, 128, 131072) > 1
+    assert mla.resolve_num_splits(3, 1000, 1, 128, 4096) == 3
+
+
 # ----------------------------------------------------------------------------- packed variable-length rows
 def _varlen_case(lens, qlens, H, seed, kv=mi.KV_BF16):
     c = mi.decode_case(len(lens), 1, H, lens, kv=kv, seed=seed)
