@@ -115,7 +115,9 @@ __device__ __forceinline__ void merge_item(const DecodeArgs& p, int64_t r, int h
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
     const int64_t n_tasks = (int64_t)a.rows * a.H * 2;
     int64_t blocks = (n_tasks + kWarps - 1) / kWarps;
-    if (a.plan_rows && blocks > 304) blocks = 304;  // grid-stride over the split rows, which are few
+    // grid-stride over the split rows: enough warps that each takes about one (row, head, half),
+    // since a task is a chain of dependent loads; with no split row every block ends at once
+    if (a.plan_rows && blocks > 1216) blocks = 1216;
     return launch_pdl(merge_kernel, dim3((unsigned)blocks), dim3(kWarps * 32), 0, s, a);
 }
 
