@@ -228,6 +228,7 @@ def _up256(x):
 @pytest.mark.parametrize("lens,Sq", [
     ("loguniform", 1),                      # the ragged workload's length mix
     ([4096] * 64, 1),                       # uniform: one unit per row
+    ([8192] * 128, 1),                      # uniform, more rows than SM pairs
     ([131072] * 4, 2),                      # few long rows: every row split evenly
     ([20000, 5, 64, 65, 300, 1], 1),        # one long row among short ones
     ([1 + (7 * i) % 500 for i in range(1100)], 1),  # more rows than the planner's threads
@@ -235,8 +236,9 @@ def _up256(x):
 ])
 def test_device_schedule_is_a_partition(lens, Sq):
     """The schedule that num_splits = -2 builds on the device, read back from the workspace: every
-    query row's visible tokens [0, n) are covered by its units exactly once and in order, the
-    partial slots are distinct, split rows are listed exactly once and their units come first."""
+    query row's visible tokens [0, n) are covered by its units exactly once and in order, a split
+    row's partial slots are consecutive, all slots are distinct, split rows are listed exactly
+    once, and the list opens with a unit of the longest length class."""
     import torch
     import mla_latent_kv_gb300 as mla
     rng = np.random.default_rng(5)
@@ -269,10 +271,10 @@ def test_device_schedule_is_a_partition(lens, Sq):
     assert np.all((units[:, 0] >= 0) & (units[:, 0] < rows))
     slots = units[units[:, 3] >= 0, 3]
     assert len(np.unique(slots)) == len(slots) and np.all(slots < max_units)
-    # units of split rows (those with partial slots) come first
-    has_slot = units[:, 3] >= 0
-    first_unsplit = count if has_slot.all() else int(np.argmin(has_slot))
-    assert has_slot[:first_unsplit].all() and not has_slot[first_unsplit:].any()
+    # longest first by length class (units of about c pages, then classes >= c/2, c/4, ...): the
+    # list opens with a unit of at least half the pages of the longest
+    unit_pages = (units[:, 2] - units[:, 1] + 63) // 64
+    assert 2 * unit_pages[0] >= unit_pages.max()
     for r in range(rows):
         b, t = divmod(r, Sq)
         n = max(0, lens[b] - (Sq - 1 - t))
